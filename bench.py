@@ -1,0 +1,431 @@
+"""Benchmark: head-major vision attention on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vattn|reference]
+                    [--workload 5] [--no-extras]
+
+A step is one call of the whole path (vattn_forward: f16 staging, Q.K^T,
+online softmax, P.V, normalise, store) over one batch of the workload.
+Metric: attention TFLOP/s = 4*B*H*N^2*D / time.  The default workload is the
+largest seeded one (B=8, H=16, N=2304 patches, D=64, keys with a shared
+per-head offset); its inputs and output (302 MB) exceed the 129 MB L2, so
+consecutive steps stream from HBM.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on
+its own GPU (the heads are independent; there is no collective on the data
+path), timing is the max over ranks and `value` counts the work of all ranks
+(weak scaling).
+
+--impl reference times the f64 CPU oracle on the host cores instead (rank 0
+only), each step a bounded sample of query rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s (4·B·H·N²·D) on 1 GB300; % of dense f16 tensor peak"
+KERNEL_SOURCES = ["vision_encoder_flash_gb300/csrc/attn_kernel.cuh",
+                  "vision_encoder_flash_gb300/csrc/ptx.cuh",
+                  "vision_encoder_flash_gb300/csrc/vattn_api.cu"]
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "vattn_fwd_kernel_b8_h16_n2304_d64.md")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+F16_OVER_BF16_NOMINAL = 1.0  # 2.25 PFLOP/s dense for both on GB300
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+        return data, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile():
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (same hash); else None."""
+    try:
+        with open(TRAFFIC_SUMMARY) as f:
+            text = f.read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []  # (host_time, sm_mhz, max_mhz, power_w, {reason: active})
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+                pw = float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else float("nan")
+            except ValueError:
+                continue
+            flags = {r: (p.lower() == "active") for r, p in zip(self.REASONS, parts[5:9])}
+            self.samples.append((time.time(), sm, mx, pw, flags))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        window = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = None
+        if not window:
+            # timed region shorter than the sampling period: nearest samples
+            window = sorted(self.samples, key=lambda s: abs(s[0] - 0.5 * (t0 + t1)))[:3]
+            note = "timed region shorter than the 100 ms sampling period; nearest samples"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        reasons = sorted({r for s in window for r, on in s[4].items() if on})
+        out = {"sm_mhz": statistics.median(s[1] for s in window),
+               "sm_max_mhz": max(s[2] for s in window), "reasons": reasons,
+               "samples": len(window),
+               "power_w_median": statistics.median(s[3] for s in window)}
+        if note:
+            out["note"] = note
+        return out
+
+
+def gpu_smi_id(torch, dev) -> str:
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    dom = getattr(props, "pci_domain_id", None)
+    pdev = getattr(props, "pci_device_id", None)
+    if bus is not None and dom is not None and pdev is not None:
+        return f"{dom:08x}:{bus:02x}:{pdev:02x}.0"
+    return str(dev.index)
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_rate(workload, q, k, v, target_s: float, max_rows=None):
+    """Time the oracle on a bounded sample of query rows; returns
+    (tflops, seconds, rows, threads)."""
+    import numpy as np
+
+    import oracle
+    threads = oracle.default_threads()
+    total = q.shape[0] * q.shape[1] * q.shape[2]
+    rng = np.random.Generator(np.random.PCG64(workload.seed))
+    probe = min(total, max(threads, 64))
+    t = time.perf_counter()
+    oracle.rows(q, k, v, rng.integers(0, total, size=probe), threads=threads)
+    per_row = (time.perf_counter() - t) / probe
+    n_rows = int(max(threads, min(total, target_s / max(per_row, 1e-9))))
+    if max_rows is not None:
+        n_rows = min(n_rows, max_rows)
+    rows = rng.integers(0, total, size=n_rows)
+    t = time.perf_counter()
+    oracle.rows(q, k, v, rows, threads=threads)
+    dt = time.perf_counter() - t
+    flops = 4.0 * n_rows * workload.n_patches * workload.head_dim
+    return flops / dt / 1e12, dt, n_rows, threads
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from vattn_inputs import make_inputs
+    q, k, v = make_inputs(workload.batch, workload.n_heads, workload.n_patches, workload.head_dim,
+                          workload.seed, workload.peaked)
+    threads = oracle.default_threads()
+    total = q.shape[0] * q.shape[1] * q.shape[2]
+    rng = np.random.Generator(np.random.PCG64(workload.seed + 1))
+    # size one step so that warmup + steps take about 60 s of host time
+    probe = max(threads, 64)
+    t = time.perf_counter()
+    oracle.rows(q, k, v, rng.integers(0, total, size=probe), threads=threads)
+    per_row = (time.perf_counter() - t) / probe
+    rows_per_step = int(max(threads, min(total, 60.0 / (args.steps + args.warmup) / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle.rows(q, k, v, rng.integers(0, total, size=rows_per_step), threads=threads)
+    samples = [rng.integers(0, total, size=rows_per_step) for _ in range(args.steps)]
+    t = time.perf_counter()
+    for rows in samples:
+        oracle.rows(q, k, v, rows, threads=threads)
+    dt = time.perf_counter() - t
+    flops = 4.0 * rows_per_step * workload.n_patches * workload.head_dim * args.steps
+    value = flops / dt / 1e12
+    sample = (f"{rows_per_step} random query rows of {total} per step (each row: all "
+              f"{workload.n_patches} keys), f64 three-pass oracle in C, {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload.name, "batch": workload.batch, "n_heads": workload.n_heads,
+                   "n_patches": workload.n_patches, "head_dim": workload.head_dim,
+                   "seed": workload.seed, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_vattn(args, workload):
+    import numpy as np
+    import torch
+
+    import vision_encoder_flash_gb300 as vef
+    from vattn_inputs import WORKLOADS, make_inputs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if pg is None:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    vef.load_library()
+    q, k, v = make_inputs(workload.batch, workload.n_heads, workload.n_patches, workload.head_dim,
+                          workload.seed + 1000 * rank, workload.peaked)
+    qd, kd, vd = (torch.from_numpy(x).to(dev) for x in (q, k, v))
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    B, H, N, D = q.shape
+    ptrs = (qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(), B, H, N, D, sp)
+
+    sampler = ClockSampler(gpu_smi_id(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+
+    # ---- warmup
+    for _ in range(args.warmup):
+        vef.forward_raw(*ptrs)
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: exactly K launches; per-launch events on the same stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    host_t0 = time.time()
+    t_all0.record(stream)
+    for s, e in ev:
+        s.record(stream)
+        vef.forward_raw(*ptrs)
+        e.record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(dev)
+    host_t1 = time.time()
+    barrier()
+    torch.cuda.synchronize(dev)
+    if vef.device_status() != 0:
+        raise RuntimeError("kernel reported a wait timeout during the timed region")
+    total_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = [s.elapsed_time(e) for s, e in ev]
+    sampler.stop()
+    clocks = sampler.summary(host_t0, host_t1)
+
+    ms_per_step = max_over_ranks(total_ms / args.steps)
+    kernel_ms = max_over_ranks(sum(launch_ms) / len(launch_ms))
+    flops = float(workload.flops)
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+
+    pk, pk_src = peaks()
+    peak_tf = float(pk["bf16_tflops"]) * F16_OVER_BF16_NOMINAL
+
+    # ---- end to end through the public API: pinned host tensors in, host out
+    e2e_steps = max(3, min(args.steps, 30))
+    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
+    oh = torch.empty(q.shape, dtype=torch.float32, pin_memory=True)
+    vef.forward(qh, kh, vh, out=oh)  # warm the allocator
+    barrier()
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    for _ in range(e2e_steps):
+        vef.forward(qh, kh, vh, out=oh)  # H2D copies, kernel, D2H copy, stream sync
+    e2e_s = max_over_ranks((time.perf_counter() - t) / e2e_steps)
+    e2e_value = flops * world / e2e_s / 1e12
+    h2d = 3 * q.nbytes
+    d2h = oh.numel() * 4
+
+    # ---- oracle on the host cores (rank 0, N = 1 only)
+    cpu_baseline = None
+    if world == 1 and not args.no_cpu_baseline:
+        tf, dt, n_rows, threads = oracle_rate(workload, q, k, v, target_s=10.0)
+        cpu_baseline = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                        "sample": f"{n_rows} random query rows of {B * H * N} (each over all {N} "
+                                  f"keys) of the same workload, f64 three-pass C oracle, "
+                                  f"{dt:.1f} s on {threads} threads"}
+
+    # ---- the other seeded workloads (context; not the bench line)
+    extras = {}
+    if not args.no_extras:
+        for idx, w in sorted(WORKLOADS.items()):
+            if w.name == workload.name:
+                continue
+            xq, xk, xv = make_inputs(w.batch, w.n_heads, w.n_patches, w.head_dim, w.seed, w.peaked)
+            xs = [torch.from_numpy(x).to(dev) for x in (xq, xk, xv)]
+            xo = torch.empty_like(xs[0])
+            xp = (xs[0].data_ptr(), xs[1].data_ptr(), xs[2].data_ptr(), xo.data_ptr(),
+                  w.batch, w.n_heads, w.n_patches, w.head_dim, sp)
+            for _ in range(10):
+                vef.forward_raw(*xp)
+            reps = 200
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                vef.forward_raw(*xp)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = a.elapsed_time(b) / reps
+            extras[w.name] = {"ms": round(ms, 5), "tflops": round(w.flops / ms / 1e9, 2),
+                              "frac_of_peak": round(w.flops / ms / 1e9 / peak_tf, 4),
+                              "l2": "hot (back-to-back, inputs may fit in L2)"}
+        if vef.device_status() != 0:
+            raise RuntimeError("kernel reported a wait timeout")
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": workload.name, "batch": B, "n_heads": H, "n_patches": N,
+                   "head_dim": D, "seed": workload.seed, "inputs": "f32 head-major, q pre-scaled",
+                   "l2": f"inputs+output {(4 * q.nbytes) / 1e6:.0f} MB per step > 129 MB L2 (no flush)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": traffic_from_profile(),
+                     "peak_source": f"{pk_src} bf16_tflops (burst) x {F16_OVER_BF16_NOMINAL} "
+                                    f"(f16/bf16 nominal ratio)",
+                     "kernel_ms": kernel_ms,
+                     "frac_of_sustained": achieved / (float(pk.get("bf16_tflops_sustained", peak_tf))
+                                                      * F16_OVER_BF16_NOMINAL)},
+        "cpu_baseline": cpu_baseline,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "path": "vision_encoder_flash_gb300.forward on pinned host tensors"},
+        "gpu_launches": args.steps,
+        "other_workloads": extras,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    from vattn_inputs import WORKLOADS
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["vattn", "reference"], default="vattn")
+    ap.add_argument("--workload", type=int, default=5, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, _, _ = dist_env()
+    if world != args.gpus:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}; using WORLD_SIZE",
+              file=sys.stderr)
+    workload = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, workload)
+    return run_vattn(args, workload)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

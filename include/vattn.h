@@ -1,0 +1,95 @@
+/*
+ * vattn.h -- C ABI of libvattn: non-causal multi-head attention over image
+ * patches, head-major layout, on one NVIDIA GB300 (sm_103a) GPU.
+ *
+ * Operation (the shader "vision_attention_flash_sub_hpd_f16.wgsl",
+ * rullama 0.1.0: its Params block, the head-major q/k/v/out buffers, the
+ * tiled online-softmax loop over keys and the final o / l store):
+ *
+ *     out[b, h, i, :] = sum_j softmax_j( q[b,h,i,:] . k[b,h,j,:] ) * v[b,h,j,:]
+ *
+ * for every batch entry b, head h and patch (query) i, the softmax running
+ * over all n_patches keys j of the same (b, h).  No 1/sqrt(head_dim) factor
+ * is applied: the caller passes q already scaled.  Like the shader, the
+ * kernel rounds q, k, v and the softmax weights to f16 for the two matrix
+ * products and keeps the softmax statistics (running max m, running sum l)
+ * and the accumulator o in f32.  The shader has no batch dimension; here
+ * batch is folded into the head index (b * n_heads + h), which is exactly
+ * how a contiguous [batch, n_heads, n_patches, head_dim] buffer is laid out.
+ *
+ * Threading: entry points are thread-safe; the last-error text is kept per
+ * host thread.
+ */
+#ifndef VATTN_H_
+#define VATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VATTN_OK = 0,
+  VATTN_ERR_INVALID_ARG = 1,    /* negative size, null pointer, aliasing out */
+  VATTN_ERR_UNSUPPORTED = 2,    /* head_dim > 128, sizes past 32-bit indexing */
+  VATTN_ERR_MISALIGNED = 3,     /* pointer not aligned to its element (4 bytes) */
+  VATTN_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+  VATTN_ERR_DEVICE_TIMEOUT = 5  /* a kernel-side wait ran out (see vattn_device_status) */
+} vattn_status;
+
+/* Largest head_dim the kernel handles. */
+#define VATTN_MAX_HEAD_DIM 128
+
+/*
+ * vattn_forward -- out = softmax(q k^T) v per (batch, head).
+ *
+ * q, k, v, out: DEVICE pointers (memory of the device current on the calling
+ *   thread) to contiguous f32 tensors of shape
+ *   [batch, n_heads, n_patches, head_dim], head-major: element (b, h, i, d)
+ *   sits at ((b * n_heads + h) * n_patches + i) * head_dim + d.  q must be
+ *   pre-scaled (typically by 1/sqrt(head_dim)).
+ * out must not overlap q, k or v.  The caller owns all four buffers; the
+ *   library keeps no reference to them after the call returns.
+ * head_dim: 1..128.  Any n_patches >= 0 (ragged tails are handled).
+ * stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *
+ * The call is asynchronous: it validates arguments, launches one kernel on
+ * `stream` and returns; the result is ready when the stream reaches that
+ * point.  It allocates no device memory.  batch*n_heads == 0 or
+ * n_patches == 0 is a successful no-op that launches nothing.
+ *
+ * Returns VATTN_OK, or an error code with no kernel launched (argument
+ * errors are detected on the host, before any CUDA call), or VATTN_ERR_CUDA
+ * if the launch itself failed.  Errors raised while the kernel runs are
+ * reported by vattn_device_status().
+ */
+vattn_status vattn_forward(const float* q, const float* k, const float* v, float* out,
+                           int64_t batch, int64_t n_heads, int64_t n_patches,
+                           int64_t head_dim, void* stream);
+
+/*
+ * vattn_device_status -- reads and clears the kernel-side error word of the
+ * current device.  Every wait inside the kernel is bounded; one that runs
+ * out sets a non-zero code (which wait, in the low byte) and the thread
+ * block ends early with its output rows unwritten.  Synchronises the
+ * current device first.  *code receives 0 when no kernel failed.
+ * Returns VATTN_OK, VATTN_ERR_DEVICE_TIMEOUT if *code != 0, or
+ * VATTN_ERR_CUDA / VATTN_ERR_INVALID_ARG.
+ */
+vattn_status vattn_device_status(uint32_t* code);
+
+/* Static text for a status code. */
+const char* vattn_status_string(vattn_status status);
+
+/* Detail text of the last error on this host thread ("" if none). */
+const char* vattn_last_error_string(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int vattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VATTN_H_ */

@@ -1,0 +1,84 @@
+"""The C-ABI library loads, exports every entry point of include/vattn.h, and
+rejects bad arguments on the host before touching CUDA (no GPU needed)."""
+import ctypes
+import subprocess
+
+import pytest
+
+import vision_encoder_flash_gb300 as vef
+from vision_encoder_flash_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from vision_encoder_flash_gb300 import build
+    build.build()
+    return vef.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _lib.exported_symbols()
+    assert set(names) == {"vattn_forward", "vattn_device_status", "vattn_status_string",
+                          "vattn_last_error_string", "vattn_version"}
+    for name in names:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    for name in names:
+        assert f" T {name}\n" in out, name
+
+
+def test_library_does_not_link_the_driver():
+    out = subprocess.run(["ldd", _lib.lib_path()], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
+
+
+def test_status_strings(lib):
+    assert vef.status_string(0) == "VATTN_OK"
+    assert vef.status_string(5) == "VATTN_ERR_DEVICE_TIMEOUT"
+    assert vef.version() == 100
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails before any CUDA call
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, -1, 2, 3, 4), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, -3, 4), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 0), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 129), 2),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 4096), 2),
+    ((0, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 4), 1),
+    ((FAKE, FAKE, FAKE, 0, 1, 2, 3, 4), 1),
+    ((FAKE + 2, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 4), 3),
+    ((FAKE, FAKE, FAKE, FAKE + 4, 1, 2, 3, 4), 1),            # out overlaps q
+    ((FAKE, FAKE, FAKE, FAKE, 1, 1, 2 ** 31, 4), 2),           # n_patches past 32 bits
+])
+def test_host_side_argument_errors(lib, args, status):
+    assert _lib.forward_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""
+
+
+@pytest.mark.parametrize("b,h,n", [(0, 4, 10), (2, 0, 10), (2, 4, 0)])
+def test_empty_problems_are_no_ops_even_with_null_pointers(lib, b, h, n):
+    assert _lib.forward_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
+
+
+def test_python_binding_rejects_bad_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 2, 3, 4)
+    with pytest.raises(TypeError):
+        vef.forward(q.double(), q, q)
+    with pytest.raises(ValueError):
+        vef.forward(q, q[:, :1], q)
+    with pytest.raises(ValueError):
+        vef.forward(q[0], q[0], q[0])
+
+
+def test_device_status_without_gpu_reports_cuda_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    code = ctypes.c_uint32(7)
+    assert lib.vattn_device_status(ctypes.byref(code)) == 4
+    assert code.value == 0

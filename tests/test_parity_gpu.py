@@ -1,0 +1,229 @@
+"""GPU parity: the CUDA path (through the C ABI) against the f64 oracle.
+
+Two bars, both against the unmodified oracle:
+
+* acceptance (the five seeded workloads and the extra cases): max
+  |gpu - oracle| <= 3e-3 and ||gpu - oracle||_2 / ||oracle||_2 <= 1e-3 on the
+  f32 inputs;
+* kernel arithmetic: the oracle evaluated on the f16-rounded q, k, v (the
+  shader vision_attention_flash_sub_hpd_f16, rullama 0.1.0, stages q, k and v
+  in f16 workgroup storage) differs from the kernel only by the f16 rounding
+  of the softmax weights P (at most 2^-11 relative per weight, so at most
+  2^-11 * max|v| per output), f32 accumulation over n_patches terms and the
+  ex2 approximation: |gpu - oracle16| <= (2^-11 + n_patches * 2^-24) * max|v|
+  + 1e-5, and rel L2 <= 5e-4.
+
+Shapes outside the seeded workloads (head_dim 1, tiny n_patches) can carry
+more f16 staging error relative to their small outputs; there the acceptance
+check uses twice the rel-L2 bar, the kernel-arithmetic check is unchanged.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import vision_encoder_flash_gb300 as vef
+from vattn_inputs import WORKLOADS, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 3e-3
+MAX_REL_L2 = 1e-3
+
+
+@pytest.fixture(scope="module")
+def torch_dev():
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("GPU tests need a CUDA device")
+    from vision_encoder_flash_gb300 import build
+    build.build()
+    vef.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    return torch, dev
+
+
+def run_gpu(torch_dev, q, k, v):
+    torch, dev = torch_dev
+    out = vef.forward(torch.from_numpy(q).to(dev), torch.from_numpy(k).to(dev),
+                      torch.from_numpy(v).to(dev))
+    torch.cuda.synchronize(dev)
+    assert vef.device_status() == 0
+    return out.cpu().numpy()
+
+
+def errors(got, ref):
+    got = got.astype(np.float64)
+    diff = got - ref
+    return float(np.abs(diff).max()), float(np.linalg.norm(diff) / max(np.linalg.norm(ref), 1e-300))
+
+
+def assert_parity(got, ref, what="", rel_l2=MAX_REL_L2):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    mx, rel = errors(got, ref)
+    assert mx <= MAX_ABS and rel <= rel_l2, f"{what}: max abs {mx:.3e}, rel L2 {rel:.3e}"
+    return mx, rel
+
+
+def f16(x):
+    return x.astype(np.float16).astype(np.float32)
+
+
+def assert_kernel_arithmetic(got, q, k, v, rows=None, what=""):
+    """GPU vs the oracle on f16-rounded inputs (see module docstring)."""
+    q16, k16, v16 = f16(q), f16(k), f16(v)
+    if rows is None:
+        ref = oracle.forward(q16, k16, v16)
+    else:
+        ref = oracle.rows(q16, k16, v16, rows)
+    n = q.shape[2]
+    bound = (2.0 ** -11 + n * 2.0 ** -24) * float(np.abs(v16).max()) + 1e-5
+    mx, rel = errors(got, ref)
+    assert mx <= bound and rel <= 5e-4, \
+        f"{what}: vs f16-input oracle max abs {mx:.3e} (bound {bound:.3e}), rel L2 {rel:.3e}"
+    return mx, rel
+
+
+# head_dim: 1..128 incl. non-multiples of 4 (plain-load variant), of 16 and
+# of 64 (two column blocks); n_patches: 1, tile edges +-1 and several tiles.
+SMALL = [(d, n) for d in (1, 3, 8, 16, 17, 32, 48, 64) for n in (1, 2, 127, 128, 129, 300)]
+SMALL += [(d, n) for d in (72, 80, 96, 100, 127, 128) for n in (1, 128, 129, 385)]
+
+
+@pytest.mark.parametrize("d,n", SMALL)
+def test_small_shapes(torch_dev, d, n):
+    q, k, v = make_inputs(2, 3, n, d, seed=1000 + 7 * d + n)
+    got = run_gpu(torch_dev, q, k, v)
+    assert_kernel_arithmetic(got, q, k, v, what=f"D={d} N={n}")
+    assert_parity(got, oracle.forward(q, k, v), f"D={d} N={n}", rel_l2=2 * MAX_REL_L2)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_workload_full(torch_dev, idx):
+    q, k, v = workload_inputs(idx)
+    got = run_gpu(torch_dev, q, k, v)
+    mx, rel = assert_parity(got, oracle.forward(q, k, v), WORKLOADS[idx].name)
+    assert_kernel_arithmetic(got, q, k, v, what=WORKLOADS[idx].name)
+    print(f"{WORKLOADS[idx].name}: max abs {mx:.3e} rel L2 {rel:.3e}")
+
+
+def test_workload_5_sampled_rows(torch_dev):
+    # full size, launch configuration of the benchmark; the oracle computes a
+    # sample of rows: every row of two heads plus 4096 rows drawn at random
+    q, k, v = workload_inputs(5)
+    got = run_gpu(torch_dev, q, k, v).reshape(-1, q.shape[-1])
+    B, H, N, D = q.shape
+    rng = np.random.Generator(np.random.PCG64(5))
+    rows = np.concatenate([np.arange(0, N), np.arange((B * H - 1) * N, B * H * N),
+                           rng.integers(0, B * H * N, size=4096)])
+    ref = oracle.rows(q, k, v, rows)
+    mx, rel = assert_parity(got[rows], ref, WORKLOADS[5].name)
+    assert_kernel_arithmetic(got[rows], q, k, v, rows=rows, what=WORKLOADS[5].name)
+    print(f"{WORKLOADS[5].name} (sampled): max abs {mx:.3e} rel L2 {rel:.3e}")
+
+
+@pytest.mark.parametrize("order", ["increasing", "decreasing", "shuffled"])
+def test_running_max_rescale_paths(torch_dev, order):
+    # scores 40*j/512 (exact in f16): increasing order raises the row max by
+    # 10 (14.4 in log2 units) on every key tile, forcing an O rescale each time
+    N, D = 1024, 64
+    j = np.arange(N)
+    if order == "decreasing":
+        j = j[::-1]
+    elif order == "shuffled":
+        j = np.random.Generator(np.random.PCG64(3)).permutation(N)
+    q = np.zeros((1, 2, N, D), np.float32)
+    q[..., 0] = 40.0
+    q[:, 1, :, 0] = np.linspace(-40, 40, N, dtype=np.float32)  # second head: mixed signs
+    k = np.zeros((1, 2, N, D), np.float32)
+    k[..., 0] = (j / 512.0).astype(np.float32)
+    v = make_inputs(1, 2, N, D, seed=77)[2]
+    assert_parity(run_gpu(torch_dev, q, k, v), oracle.forward(q, k, v), order)
+
+
+def test_single_patch_returns_v_rounded(torch_dev):
+    q, k, v = make_inputs(1, 4, 1, 64, seed=11)
+    got = run_gpu(torch_dev, q * 50, k, v)
+    # P = 1 exactly after f16 rounding; l sums the unrounded exp2 of a ~1e-6
+    # residual (s*log2e - round(s*log2e)), hence a relative error of ~1e-6
+    np.testing.assert_allclose(got, v.astype(np.float16).astype(np.float32), rtol=1e-5, atol=0)
+
+
+def test_identical_keys_give_mean(torch_dev):
+    q, k, v = make_inputs(1, 2, 333, 64, seed=12)
+    k[:] = k[:, :, :1]
+    assert_parity(run_gpu(torch_dev, q, k, v),
+                  np.broadcast_to(v.astype(np.float64).mean(axis=2, keepdims=True), q.shape), "mean")
+
+
+def test_joint_permutation(torch_dev):
+    q, k, v = make_inputs(1, 2, 700, 72, seed=13)
+    perm = np.random.Generator(np.random.PCG64(13)).permutation(700)
+    a = run_gpu(torch_dev, q, k, v)
+    b = run_gpu(torch_dev, q, np.ascontiguousarray(k[:, :, perm]), np.ascontiguousarray(v[:, :, perm]))
+    assert_parity(b, a.astype(np.float64), "permutation")
+
+
+def test_deterministic(torch_dev):
+    q, k, v = make_inputs(2, 4, 513, 64, seed=14)
+    a = run_gpu(torch_dev, q, k, v)
+    b = run_gpu(torch_dev, q, k, v)
+    np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("d,n", [(64, 200), (72, 129), (17, 130)])
+def test_no_store_past_the_last_patch(torch_dev, d, n):
+    # out is a view followed by sentinel memory: rows >= n must stay untouched
+    torch, dev = torch_dev
+    q, k, v = make_inputs(1, 1, n, d, seed=15)
+    buf = torch.full((n * d + 4096,), 12345.0, device=dev)
+    qd, kd, vd = (torch.from_numpy(x).to(dev) for x in (q, k, v))
+    vef.forward_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), buf.data_ptr(), 1, 1, n, d,
+                    torch.cuda.current_stream(dev).cuda_stream)
+    torch.cuda.synchronize(dev)
+    host = buf.cpu().numpy()
+    assert np.all(host[n * d:] == 12345.0)
+    assert_parity(host[:n * d].reshape(1, 1, n, d), oracle.forward(q, k, v), "sentinel")
+
+
+def test_unaligned_pointers_take_the_plain_load_path(torch_dev):
+    # 4-byte but not 16-byte aligned bases: TMA cannot be used
+    torch, dev = torch_dev
+    shape = (1, 2, 257, 64)
+    q, k, v = make_inputs(*shape, seed=16)
+    numel = q.size
+    ts = []
+    for x in (q, k, v):
+        t = torch.zeros(numel + 1, device=dev)
+        t[1:] = torch.from_numpy(x.ravel()).to(dev)
+        ts.append(t)
+    out = torch.zeros(numel + 1, device=dev)
+    vef.forward_raw(ts[0].data_ptr() + 4, ts[1].data_ptr() + 4, ts[2].data_ptr() + 4,
+                    out.data_ptr() + 4, *shape, torch.cuda.current_stream(dev).cuda_stream)
+    torch.cuda.synchronize(dev)
+    got = out[1:].cpu().numpy().reshape(shape)
+    assert_parity(got, oracle.forward(q, k, v), "unaligned")
+
+
+def test_side_stream_and_empty(torch_dev):
+    torch, dev = torch_dev
+    q, k, v = make_inputs(1, 2, 300, 32, seed=17)
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        qd, kd, vd = (torch.from_numpy(x).to(dev) for x in (q, k, v))
+        out = vef.forward(qd, kd, vd, stream=s)
+    s.synchronize()
+    assert_parity(out.cpu().numpy(), oracle.forward(q, k, v), "side stream")
+    z = torch.zeros(0, 2, 5, 8, device=dev)
+    assert vef.forward(z, z, z).shape == z.shape
+    z = torch.zeros(1, 2, 0, 8, device=dev)
+    assert vef.forward(z, z, z).shape == z.shape
+
+
+def test_host_tensors_round_trip(torch_dev):
+    torch, _ = torch_dev
+    q, k, v = make_inputs(1, 2, 130, 64, seed=18)
+    pin = lambda x: torch.from_numpy(x).pin_memory()
+    out = vef.forward(pin(q), pin(k), pin(v))
+    assert out.device.type == "cpu"
+    assert_parity(out.numpy(), oracle.forward(q, k, v), "host tensors")

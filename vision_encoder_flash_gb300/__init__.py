@@ -1,0 +1,75 @@
+"""vision_encoder_flash_gb300 -- head-major vision attention on GB300 (sm_103a).
+
+``forward(q, k, v)`` computes ``softmax(q @ k^T) @ v`` per (batch, head) for
+f32 tensors of shape ``[batch, n_heads, n_patches, head_dim]`` (q already
+scaled by the caller), through the C ABI of ``libvattn.so`` (include/vattn.h).
+This module only marshals arguments: every step of the computation runs in
+the library's CUDA kernel.  There is no CPU fallback; if the library is
+missing or no GPU is present the calls raise.
+"""
+from __future__ import annotations
+
+from ._lib import (VattnError, device_status, exported_symbols, forward_raw, lib_path,
+                   load_library, status_string, version)
+
+__all__ = ["forward", "forward_raw", "device_status", "VattnError", "load_library",
+           "lib_path", "exported_symbols", "status_string", "version"]
+
+
+def forward(q, k, v, out=None, stream=None):
+    """out = softmax(q k^T) v for torch f32 tensors ``[B, H, N, D]``.
+
+    CUDA tensors: runs on their device and on ``stream`` (default: the
+    current torch stream); returns ``out`` without synchronising.
+
+    CPU tensors: copies q, k, v to the current CUDA device, runs the kernel,
+    copies the result back into ``out`` (or a new pinned tensor) and
+    synchronises that stream before returning.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32, got {t.dtype}")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [batch, n_heads, n_patches, head_dim]")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must be on the same device")
+
+    if q.device.type == "cpu":
+        dev = torch.device("cuda", torch.cuda.current_device())
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        with torch.cuda.stream(s):
+            qd = q.to(dev, non_blocking=True)
+            kd = k.to(dev, non_blocking=True)
+            vd = v.to(dev, non_blocking=True)
+            od = torch.empty_like(qd)
+            _launch(qd, kd, vd, od, s)
+            if out is None:
+                out = torch.empty(q.shape, dtype=torch.float32, pin_memory=True)
+            out.copy_(od, non_blocking=True)
+        s.synchronize()
+        return out
+
+    if q.device.type != "cuda":
+        raise ValueError(f"unsupported device {q.device}")
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    _launch(q, k, v, out, s)
+    return out
+
+
+def _launch(q, k, v, out, stream):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (head-major [B, H, N, D])")
+    if out.shape != q.shape or out.dtype != q.dtype or out.device != q.device:
+        raise ValueError("out must match q in shape, dtype and device")
+    B, H, N, D = q.shape
+    forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D,
+                stream.cuda_stream)

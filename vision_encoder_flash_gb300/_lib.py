@@ -1,0 +1,95 @@
+"""ctypes binding of libvattn.so: same entry points as include/vattn.h."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+HEADER = os.path.join(_ROOT, "include", "vattn.h")
+
+_STATUS = {0: "VATTN_OK", 1: "VATTN_ERR_INVALID_ARG", 2: "VATTN_ERR_UNSUPPORTED",
+           3: "VATTN_ERR_MISALIGNED", 4: "VATTN_ERR_CUDA", 5: "VATTN_ERR_DEVICE_TIMEOUT"}
+
+_LIB = None
+
+
+class VattnError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{_STATUS.get(status, status)}: {detail}")
+
+
+def lib_path() -> str:
+    return os.environ.get("VATTN_LIB", os.path.join(_PKG, "libvattn.so"))
+
+
+def load_library():
+    """Load libvattn.so (built by vision_encoder_flash_gb300/build.py); raises if absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} not found: build it with `python -c \"import __graft_entry__ as g; "
+                          f"g.build()\"` (there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.vattn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.vattn_forward.restype = ctypes.c_int
+    lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.vattn_device_status.restype = ctypes.c_int
+    lib.vattn_status_string.argtypes = [ctypes.c_int]
+    lib.vattn_status_string.restype = ctypes.c_char_p
+    lib.vattn_last_error_string.argtypes = []
+    lib.vattn_last_error_string.restype = ctypes.c_char_p
+    lib.vattn_version.argtypes = []
+    lib.vattn_version.restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        detail = load_library().vattn_last_error_string().decode(errors="replace")
+        raise VattnError(status, detail)
+
+
+def forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int, n_heads: int,
+                n_patches: int, head_dim: int, stream: int = 0) -> None:
+    """Direct call of vattn_forward with device addresses (ints) and a stream handle."""
+    _check(load_library().vattn_forward(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches,
+                                        head_dim, stream))
+
+
+def forward_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,
+                   stream=0) -> int:
+    """Like forward_raw but returns the status code instead of raising."""
+    return int(load_library().vattn_forward(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                            n_patches, head_dim, stream))
+
+
+def device_status() -> int:
+    """Read-and-clear the kernel-side error word (synchronises the device)."""
+    code = ctypes.c_uint32(0)
+    status = load_library().vattn_device_status(ctypes.byref(code))
+    if status not in (0, 5):
+        _check(status)
+    return int(code.value)
+
+
+def status_string(status: int) -> str:
+    return load_library().vattn_status_string(status).decode()
+
+
+def version() -> int:
+    return int(load_library().vattn_version())
+
+
+def exported_symbols() -> list[str]:
+    """Function names declared in include/vattn.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vattn_[a-z_]+)\s*\(", text)))

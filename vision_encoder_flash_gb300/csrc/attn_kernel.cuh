@@ -1,0 +1,550 @@
+// attn_kernel.cuh -- head-major non-causal attention forward for sm_103a.
+//
+// Computes, per (batch*head) bh and query row i,
+//     out[bh, i, :] = sum_j softmax_j(q[bh,i,:] . k[bh,j,:]) v[bh, j, :]
+// as in the WGSL shader "vision_attention_flash_sub_hpd_f16.wgsl"
+// (rullama 0.1.0): q/k/v staged to f16, scores and P.V accumulated in f32,
+// f32 online softmax with running (m, l, o), no 1/sqrt(head_dim) factor.
+//
+// The shader's design (8 queries x 32 keys per 64-thread workgroup, scalar
+// dot products, subgroup reductions) is replaced by a GB300 one:
+//   * one thread block = one bh and NQ query tiles of 128 rows;
+//   * warp 0 streams f32 Q/K/V tiles into a ring of shared-memory slots
+//     with TMA (cp.async.bulk.tensor), out-of-range rows/columns read as 0;
+//   * "converter" warps turn each f32 tile into f16 in the 128-byte-swizzled
+//     layout the tensor core reads (the shader's f32 -> f16 staging);
+//   * warp 1 issues tcgen05.mma: S = Q K^T (f32 in TMEM), then O += P V with
+//     P taken from TMEM (it overwrites S in place) and V from shared memory;
+//   * one warpgroup per query tile runs the online softmax: thread = query
+//     row, so the row max and row sum need no shuffles; exp is exp2 with
+//     log2(e) folded into one FMA; O is rescaled in TMEM only when the
+//     row max grew by more than 2^8 (exact after the final 1/l);
+//   * the same warpgroup divides by l and stores its rows of out.
+// Every wait is bounded: on timeout the block records the wait site in
+// g_vattn_status, raises a shared abort flag so the other roles leave their
+// loops, drains its own TMA copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace vattn {
+
+constexpr int kBM = 128;          // query rows per tile (UMMA M)
+constexpr int kBN = 128;          // keys per K/V tile (UMMA N of S, K of P.V)
+constexpr int kThreads = 512;     // 16 warps
+constexpr int kSlotBytes = 32768; // one f32 staging slot
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;                 // lazy-rescale threshold
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
+
+// g_vattn_status: bit 8 = a wait timed out; low byte = the wait site.
+enum WaitSite : uint32_t {
+  kSiteProducerSlot = 1,
+  kSiteConvSlot = 2,
+  kSiteConvKStage = 3,
+  kSiteConvVStage = 4,
+  kSiteMmaQ = 5,
+  kSiteMmaK = 6,
+  kSiteMmaV = 7,
+  kSiteMmaP = 8,
+  kSiteSoftS = 9,
+  kSiteSoftO = 10,
+  kSiteEpilogue = 11,
+  kSiteDrainTma = 12,
+  kSiteDrainMma = 13,
+};
+constexpr uint32_t kStatusTimeout = 0x100u;
+
+__device__ uint32_t g_vattn_status;
+
+struct Params {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  int n_patches;  // N
+  int head_dim;   // D
+  int d_pad;      // D rounded up to 16
+  int n_qblocks;  // thread blocks per bh
+  int n_ktiles;   // ceil(N / kBN)
+  int vec_out;    // out rows may be written with 16-byte stores
+};
+
+// Shared-memory plan for NQ query tiles and NKB 64-column blocks of head_dim.
+// f16 tiles: NKB blocks of [128 rows x 128 bytes], 128-byte swizzle.
+template <int NQ, int NKB>
+struct Plan {
+  static constexpr int kSlotRows = NKB == 1 ? 128 : 64;  // rows per f32 slot
+  static constexpr int kSubs = 128 / kSlotRows;          // slots per tile
+  static constexpr int kTileF16 = NKB * 128 * 128;
+  static constexpr int kF32Slots = NKB == 1 ? 4 : 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + NQ * kTileF16;
+  static constexpr int kOffV = kOffK + 2 * kTileF16;
+  static constexpr int kOffF32 = kOffV + 2 * kTileF16;
+  static constexpr int kOffBar = kOffF32 + kF32Slots * kSlotBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  static constexpr int kConvWarps = 16 - 2 - 4 * NQ;
+  static constexpr int kConvThreads = kConvWarps * 32;
+  static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
+};
+
+// mbarrier indices inside the barrier block.
+enum Bar : int {
+  kBarF32Full = 0,    // [4] TMA landed in slot
+  kBarF32Empty = 4,   // [4] converters done reading slot
+  kBarKFull = 8,      // [2] f16 K stage written
+  kBarKEmpty = 10,    // [2] S MMAs done with K stage
+  kBarVFull = 12,     // [2] f16 V stage written
+  kBarVEmpty = 14,    // [2] P.V MMAs done with V stage
+  kBarQFull = 16,     // f16 Q tiles written
+  kBarSFull = 17,     // [2] S tile complete in TMEM
+  kBarPFull = 19,     // [2] P written to TMEM and O rescaled (per query tile)
+  kBarODone = 21,     // [2] P.V complete (per query tile)
+  kBarMmaDone = 23,   // every MMA of the block complete
+  kNumBars = 24,
+};
+constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
+constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
+
+struct Waiter {
+  volatile uint32_t* abort_flag;
+
+  // Bounded wait that also gives up when another role has aborted.
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t site) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if ((it & 31u) == 0) {
+        if (*abort_flag) return false;
+        if (ptx::global_timer_ns() - t0 > kWaitTimeoutNs) {
+          *abort_flag = 1;
+          atomicOr(&g_vattn_status, kStatusTimeout | site);
+          return false;
+        }
+      }
+    }
+  }
+
+  // Warp-uniform variant: all lanes leave together.
+  __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, uint32_t site) const {
+    const bool ok = wait(bar, parity, site);
+    return __all_sync(0xffffffffu, ok);
+  }
+
+  // Bounded wait that ignores the abort flag: used while draining copies
+  // and MMAs before the block exits.
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, uint32_t site) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if ((it & 31u) == 0 && ptx::global_timer_ns() - t0 > kWaitTimeoutNs) {
+        atomicOr(&g_vattn_status, kStatusTimeout | site);
+        return false;
+      }
+    }
+  }
+};
+
+// f16 tile address of element chunk (row R, 8-column chunk c): block c/8 of
+// 128 rows x 128 bytes; 16-byte chunk (c%8) ^ (R%8) within the row.
+__device__ __forceinline__ uint32_t f16_chunk_offset(int R, int c) {
+  return static_cast<uint32_t>((c >> 3) * (128 * 128) + R * 128 + (((c & 7) ^ (R & 7)) << 4));
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+  uint4 h;
+  h.x = ptx::pack_half2(x[0], x[1]);
+  h.y = ptx::pack_half2(x[2], x[3]);
+  h.z = ptx::pack_half2(x[4], x[5]);
+  h.w = ptx::pack_half2(x[6], x[7]);
+  return h;
+}
+
+// f32 slot (rows x d_pad, dense) -> f16 tile rows [row_base, row_base+rows).
+template <int CT>
+__device__ __forceinline__ void convert_slot(const float* src, uint8_t* dst, int row_base,
+                                             int rows, int d_pad, int ct) {
+  const int cpr = d_pad >> 3;
+  const int dr = CT / cpr, dc = CT % cpr;
+  int r = ct / cpr, c = ct % cpr;
+  while (r < rows) {
+    const float* s = src + r * d_pad + c * 8;
+    // threads with (c & 4) read their upper half first: the 8 threads of a
+    // shared-memory phase then touch all 32 banks once
+    const int sw = (c & 4);
+    const float4 x0 = *reinterpret_cast<const float4*>(s + sw);
+    const float4 x1 = *reinterpret_cast<const float4*>(s + (4 - sw));
+    const float4 a = sw ? x1 : x0;
+    const float4 b = sw ? x0 : x1;
+    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    *reinterpret_cast<uint4*>(dst + f16_chunk_offset(row_base + r, c)) = pack8(x);
+    r += dr;
+    c += dc;
+    if (c >= cpr) {
+      c -= cpr;
+      ++r;
+    }
+  }
+}
+
+// Global f32 rows (any head_dim, 4-byte aligned) -> f16 tile, zero padding.
+template <int CT>
+__device__ __forceinline__ void convert_global(const float* g, int grow0, int n_rows_valid,
+                                               int D, uint8_t* dst, int d_pad, int ct) {
+  const int cpr = d_pad >> 3;
+  const int dr = CT / cpr, dc = CT % cpr;
+  int r = ct / cpr, c = ct % cpr;
+  while (r < 128) {
+    float x[8];
+    const bool row_ok = r < n_rows_valid;
+    const float* s = g + static_cast<size_t>(grow0 + r) * D;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int d = c * 8 + e;
+      x[e] = (row_ok && d < D) ? __ldg(s + d) : 0.0f;
+    }
+    *reinterpret_cast<uint4*>(dst + f16_chunk_offset(r, c)) = pack8(x);
+    r += dr;
+    c += dc;
+    if (c >= cpr) {
+      c -= cpr;
+      ++r;
+    }
+  }
+}
+
+template <int NQ, int NKB, bool kTma>
+__global__ void __launch_bounds__(kThreads, 1)
+    vattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using P = Plan<NQ, NKB>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = ptx::smem_addr(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+  uint8_t* const base = smem_raw + (base_s - raw_s);
+  const uint32_t bar0 = base_s + P::kOffBar;
+  auto bar = [bar0](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(base + P::kOffBar + kAbortOff);
+  const Waiter w{abort_flag};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / p.n_qblocks;
+  const int q_row0 = (blockIdx.x % p.n_qblocks) * (kBM * NQ);
+  const int N = p.n_patches;
+  const int T = p.n_ktiles;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < P::kF32Slots; ++i) {
+      ptx::mbar_init(bar(kBarF32Full + i), 1);
+      ptx::mbar_init(bar(kBarF32Empty + i), P::kConvThreads);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(kBarKFull + i), P::kConvThreads);
+      ptx::mbar_init(bar(kBarKEmpty + i), 1);
+      ptx::mbar_init(bar(kBarVFull + i), P::kConvThreads);
+      ptx::mbar_init(bar(kBarVEmpty + i), 1);
+      ptx::mbar_init(bar(kBarSFull + i), 1);
+      ptx::mbar_init(bar(kBarPFull + i), 128);
+      ptx::mbar_init(bar(kBarODone + i), 1);
+    }
+    ptx::mbar_init(bar(kBarQFull), P::kConvThreads);
+    ptx::mbar_init(bar(kBarMmaDone), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(bar0 + kTmemSlotOff, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + P::kOffBar + kTmemSlotOff);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (kTma && lane == 0) {
+      ptx::prefetch_tensormap(&tm_q);
+      ptx::prefetch_tensormap(&tm_k);
+      ptx::prefetch_tensormap(&tm_v);
+      const uint32_t slot_bytes = static_cast<uint32_t>(P::kSlotRows * p.d_pad * 4);
+      int load = 0;
+      bool ok = true;
+      auto issue = [&](const CUtensorMap* tm, int row) {
+        const int slot = load % P::kF32Slots;
+        const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
+        if (!w.wait(bar(kBarF32Empty + slot), (use & 1u) ^ 1u, kSiteProducerSlot)) {
+          ok = false;
+          return;
+        }
+        ptx::mbar_arrive_expect_tx(bar(kBarF32Full + slot), slot_bytes);
+        ptx::tma_load_3d(base_s + P::kOffF32 + slot * kSlotBytes, tm, bar(kBarF32Full + slot), 0,
+                         row, bh);
+        ++load;
+      };
+      for (int t = 0; ok && t < NQ; ++t)
+        for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_q, q_row0 + t * kBM + s * P::kSlotRows);
+      for (int j = 0; ok && j < T; ++j) {
+        for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_k, j * kBN + s * P::kSlotRows);
+        for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_v, j * kBN + s * P::kSlotRows);
+      }
+      // the newest copy into each slot must have landed before exit
+      for (int slot = 0; slot < P::kF32Slots; ++slot) {
+        if (load > slot) {
+          const int uses = (load - 1 - slot) / P::kF32Slots + 1;
+          w.drain(bar(kBarF32Full + slot), static_cast<uint32_t>(uses - 1) & 1u, kSiteDrainTma);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = ptx::idesc_f16_f32(kBM, kBN, false);
+      const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
+      const int ksteps = p.d_pad >> 4;
+      auto s_col = [](int t, int j) -> uint32_t {
+        return NQ == 2 ? static_cast<uint32_t>(t) * 128u : static_cast<uint32_t>(j & 1) * 128u;
+      };
+      auto issue_s = [&](int t, int j) {
+        const uint32_t qa = base_s + P::kOffQ + t * P::kTileF16;
+        const uint32_t kb = base_s + P::kOffK + (j & 1) * P::kTileF16;
+        const uint32_t d = tmem + s_col(t, j);
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const uint32_t off = static_cast<uint32_t>((ks >> 2) * (128 * 128) + (ks & 3) * 32);
+          ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
+                      ptx::smem_desc(kb + off, 16, 1024, ptx::kSwizzle128B), idesc_s,
+                      ks > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(kBarSFull + (NQ == 2 ? t : (j & 1))));
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vb = base_s + P::kOffV + (j & 1) * P::kTileF16;
+        const uint32_t d = tmem + 256u + static_cast<uint32_t>(t) * 128u;
+        const uint32_t a = tmem + s_col(t, j);
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
+                      ptx::smem_desc(vb + ks * 2048, 128 * 128, 1024, ptx::kSwizzle128B),
+                      idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(kBarODone + t));
+      };
+
+      bool ok = w.wait(bar(kBarQFull), 0, kSiteMmaQ) && w.wait(bar(kBarKFull), 0, kSiteMmaK);
+      if (ok) {
+        ptx::tc_fence_after();
+        for (int t = 0; t < NQ; ++t) issue_s(t, 0);
+        ptx::mma_commit(bar(kBarKEmpty));
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        const uint32_t st = static_cast<uint32_t>(j & 1);
+        const uint32_t nst = st ^ 1u;
+        const uint32_t nph = static_cast<uint32_t>((j + 1) >> 1) & 1u;
+        if (NQ == 1) {
+          if (j + 1 < T) {
+            if (!(ok = w.wait(bar(kBarKFull + nst), nph, kSiteMmaK))) break;
+            ptx::tc_fence_after();
+            issue_s(0, j + 1);
+            ptx::mma_commit(bar(kBarKEmpty + nst));
+          }
+          if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
+          if (!(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
+            break;
+          ptx::tc_fence_after();
+          issue_pv(0, j);
+          ptx::mma_commit(bar(kBarVEmpty + st));
+        } else {
+          for (int t = 0; t < NQ; ++t) {
+            if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
+            if (t == 0 &&
+                !(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
+              break;
+            ptx::tc_fence_after();
+            issue_pv(t, j);
+            if (t == NQ - 1) ptx::mma_commit(bar(kBarVEmpty + st));
+            if (j + 1 < T) {
+              if (t == 0 && !(ok = w.wait(bar(kBarKFull + nst), nph, kSiteMmaK))) break;
+              ptx::tc_fence_after();
+              issue_s(t, j + 1);
+              if (t == NQ - 1) ptx::mma_commit(bar(kBarKEmpty + nst));
+            }
+          }
+        }
+      }
+      ptx::mma_commit(bar(kBarMmaDone));
+    }
+  } else if (warp >= 4 && warp < 4 + 4 * NQ) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t o_addr = tmem + lane_addr + 256u + static_cast<uint32_t>(t) * 128u;
+    float m_ref = -INFINITY;  // running max in log2 units (may lag the true max by < 8)
+    float l = 0.0f;           // running sum of exp2(s*log2e - m_ref)
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const int buf = NQ == 2 ? t : (j & 1);
+      const uint32_t par = NQ == 2 ? (static_cast<uint32_t>(j) & 1u)
+                                   : (static_cast<uint32_t>(j >> 1) & 1u);
+      if (!(ok = w.wait_warp(bar(kBarSFull + buf), par, kSiteSoftS))) break;
+      ptx::tc_fence_after();
+      const uint32_t s_addr = tmem + lane_addr + static_cast<uint32_t>(buf) * 128u;
+      const int valid = min(kBN, N - j * kBN);
+
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, r);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float s = (c * 32 + i < valid) ? __uint_as_float(r[i]) : -INFINITY;
+          mx = fmaxf(mx, s);
+        }
+      }
+      const float mt = mx * kLog2e;
+      const bool need = mt > m_ref + kRescaleLog2;
+      const float m_new = need ? mt : m_ref;
+      const float alpha = ptx::ex2_approx(m_ref - m_new);  // 0 on the first tile, 1 if kept
+      l *= alpha;
+      m_ref = m_new;
+
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, r);
+        ptx::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int col = c * 32 + 2 * i;
+          const float s0 = col < valid ? __uint_as_float(r[2 * i]) : -INFINITY;
+          const float s1 = col + 1 < valid ? __uint_as_float(r[2 * i + 1]) : -INFINITY;
+          const float p0 = ptx::ex2_approx(fmaf(s0, kLog2e, -m_ref));
+          const float p1 = ptx::ex2_approx(fmaf(s1, kLog2e, -m_ref));
+          l += p0 + p1;
+          pk[i] = ptx::pack_half2(p0, p1);
+        }
+        // P (f16 pairs) overwrites S columns [16c, 16c+16), all already read
+        ptx::tmem_st_32x32b_x16(s_addr + c * 16, pk);
+      }
+
+      if (j > 0) {
+        if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(j - 1) & 1u, kSiteSoftO)))
+          break;
+        if (__any_sync(0xffffffffu, need)) {
+          ptx::tc_fence_after();
+          for (int c = 0; c < (p.d_pad >> 4); ++c) {
+            uint32_t y[16];
+            ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
+            ptx::tmem_st_32x32b_x16(o_addr + c * 16, y);
+          }
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(kBarPFull + t));
+    }
+    if (ok && w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(T - 1) & 1u, kSiteEpilogue)) {
+      ptx::tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const int row = q_row0 + t * kBM + quarter * 32 + lane;
+      const int D = p.head_dim;
+      float* orow = p.out + (static_cast<size_t>(bh) * N + row) * D;
+      for (int c = 0; c < (p.d_pad >> 4); ++c) {
+        uint32_t y[16];
+        ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
+        ptx::tmem_wait_ld();
+        if (row < N) {
+          if (p.vec_out) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const int d = c * 16 + v4 * 4;
+              if (d < D) {
+                float4 o;
+                o.x = __uint_as_float(y[4 * v4 + 0]) * inv_l;
+                o.y = __uint_as_float(y[4 * v4 + 1]) * inv_l;
+                o.z = __uint_as_float(y[4 * v4 + 2]) * inv_l;
+                o.w = __uint_as_float(y[4 * v4 + 3]) * inv_l;
+                *reinterpret_cast<float4*>(orow + d) = o;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int d = c * 16 + i;
+              if (d < D) orow[d] = __uint_as_float(y[i]) * inv_l;
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ converters
+    const int ct = (warp < 4 ? warp - 2 : warp - 2 - 4 * NQ) * 32 + lane;
+    constexpr int CT = P::kConvThreads;
+    const size_t head_off = static_cast<size_t>(bh) * N * p.head_dim;
+    int load = 0;
+    bool ok = true;
+    // one 128-row tile (f32 source rows tile_row0..) into the f16 tile at dst
+    auto tile = [&](const float* g, int tile_row0, uint8_t* dst) {
+      if (kTma) {
+        for (int s = 0; s < P::kSubs; ++s) {
+          const int slot = load % P::kF32Slots;
+          const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
+          if (!(ok = w.wait(bar(kBarF32Full + slot), use & 1u, kSiteConvSlot))) return;
+          convert_slot<CT>(reinterpret_cast<const float*>(base + P::kOffF32 + slot * kSlotBytes),
+                           dst, s * P::kSlotRows, P::kSlotRows, p.d_pad, ct);
+          ptx::mbar_arrive(bar(kBarF32Empty + slot));
+          ++load;
+        }
+      } else {
+        convert_global<CT>(g + head_off, tile_row0, N - tile_row0, p.head_dim, dst, p.d_pad, ct);
+      }
+    };
+    for (int t = 0; ok && t < NQ; ++t) tile(p.q, q_row0 + t * kBM, base + P::kOffQ + t * P::kTileF16);
+    if (ok) {
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(bar(kBarQFull));
+    }
+    for (int j = 0; ok && j < T; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u;
+      if (!(ok = w.wait(bar(kBarKEmpty + st), ph, kSiteConvKStage))) break;
+      tile(p.k, j * kBN, base + P::kOffK + st * P::kTileF16);
+      if (!ok) break;
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(bar(kBarKFull + st));
+      if (!(ok = w.wait(bar(kBarVEmpty + st), ph, kSiteConvVStage))) break;
+      tile(p.v, j * kBN, base + P::kOffV + st * P::kTileF16);
+      if (!ok) break;
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(bar(kBarVFull + st));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) w.drain(bar(kBarMmaDone), 0, kSiteDrainMma);
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace vattn

@@ -1,0 +1,232 @@
+// vattn_api.cu -- the C ABI declared in include/vattn.h: argument checks,
+// tensor-map encoding, variant choice and launch of the sm_103a kernel.
+//
+// The operation is the one of the WGSL shader
+// "vision_attention_flash_sub_hpd_f16.wgsl" (rullama 0.1.0): its Params block
+// (head_dim, n_heads, n_patches) becomes plain integer arguments plus a
+// batch size folded into the head index; its four storage buffers become
+// device pointers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/vattn.h"
+#include "attn_kernel.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+vattn_status fail(vattn_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+vattn_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(VATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time so that the
+// library itself does not link against libcuda.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+cudaError_t g_encode_err = cudaSuccess;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                    cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// 3-D view {head_dim, n_patches, batch*n_heads} of a head-major f32 tensor;
+// one box = slot_rows rows x d_pad columns; out-of-range elements read 0.
+vattn_status make_tmap(CUtensorMap* tm, const float* ptr, int64_t bh, int64_t n, int64_t d,
+                       int d_pad, int slot_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    if (g_encode_err != cudaSuccess) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
+    return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                              static_cast<cuuint64_t>(bh)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4u,
+                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(d) * 4u};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d_pad), static_cast<cuuint32_t>(slot_rows), 1u};
+  const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims,
+                         strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult %d", static_cast<int>(r));
+  return VATTN_OK;
+}
+
+constexpr int kMaxDevices = 64;
+
+template <int NQ, int NKB, bool kTma>
+vattn_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                    const vattn::Params& p, unsigned grid, cudaStream_t stream, int device) {
+  using P = vattn::Plan<NQ, NKB>;
+  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kTma>;
+  static std::atomic<uint8_t> configured[kMaxDevices];
+  if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
+  if (!configured[device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         P::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    configured[device].store(1, std::memory_order_release);
+  }
+  kernel<<<grid, vattn::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return VATTN_OK;
+}
+
+bool overlaps(const void* a, const void* b, uint64_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+vattn_status vattn_forward(const float* q, const float* k, const float* v, float* out,
+                           int64_t batch, int64_t n_heads, int64_t n_patches, int64_t head_dim,
+                           void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks, before any CUDA call
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
+                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (head_dim > VATTN_MAX_HEAD_DIM)
+    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
+  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
+  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+
+  const int D = static_cast<int>(head_dim);
+  const int N = static_cast<int>(n_patches);
+  const int d_pad = (D + 15) & ~15;
+  const int nkb = d_pad <= 64 ? 1 : 2;
+  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+  // TMA needs 16-byte aligned bases and row strides (head_dim % 4 == 0)
+  const bool tma = (D % 4 == 0) &&
+                   ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                     reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+
+  vattn::Params p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = d_pad;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+
+  // ---- device side
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+  CUtensorMap tq, tk, tv;
+  std::memset(&tq, 0, sizeof(tq));
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  const int slot_rows = nkb == 1 ? vattn::Plan<1, 1>::kSlotRows : vattn::Plan<1, 2>::kSlotRows;
+  if (tma) {
+    vattn_status st;
+    if ((st = make_tmap(&tq, q, bh, N, D, d_pad, slot_rows)) != VATTN_OK) return st;
+    if ((st = make_tmap(&tk, k, bh, N, D, d_pad, slot_rows)) != VATTN_OK) return st;
+    if ((st = make_tmap(&tv, v, bh, N, D, d_pad, slot_rows)) != VATTN_OK) return st;
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const unsigned g = static_cast<unsigned>(grid);
+  if (nkb == 1 && nq == 2)
+    return tma ? launch<2, 1, true>(tq, tk, tv, p, g, stream, device)
+               : launch<2, 1, false>(tq, tk, tv, p, g, stream, device);
+  if (nkb == 1)
+    return tma ? launch<1, 1, true>(tq, tk, tv, p, g, stream, device)
+               : launch<1, 1, false>(tq, tk, tv, p, g, stream, device);
+  return tma ? launch<1, 2, true>(tq, tk, tv, p, g, stream, device)
+             : launch<1, 2, false>(tq, tk, tv, p, g, stream, device);
+}
+
+vattn_status vattn_device_status(uint32_t* code) {
+  g_last_error[0] = '\0';
+  if (!code) return fail(VATTN_ERR_INVALID_ARG, "null code pointer");
+  *code = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  uint32_t value = 0;
+  e = cudaMemcpyFromSymbol(&value, vattn::g_vattn_status, sizeof(value));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (value != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(vattn::g_vattn_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+  }
+  *code = value;
+  if (value != 0)
+    return fail(VATTN_ERR_DEVICE_TIMEOUT, "a kernel wait timed out (status 0x%x, site %u)", value,
+                value & 0xFFu);
+  return VATTN_OK;
+}
+
+const char* vattn_status_string(vattn_status status) {
+  switch (status) {
+    case VATTN_OK: return "VATTN_OK";
+    case VATTN_ERR_INVALID_ARG: return "VATTN_ERR_INVALID_ARG";
+    case VATTN_ERR_UNSUPPORTED: return "VATTN_ERR_UNSUPPORTED";
+    case VATTN_ERR_MISALIGNED: return "VATTN_ERR_MISALIGNED";
+    case VATTN_ERR_CUDA: return "VATTN_ERR_CUDA";
+    case VATTN_ERR_DEVICE_TIMEOUT: return "VATTN_ERR_DEVICE_TIMEOUT";
+  }
+  return "VATTN_ERR_UNKNOWN";
+}
+
+const char* vattn_last_error_string(void) { return g_last_error; }
+
+int vattn_version(void) { return 100; }
+
+}  // extern "C"
