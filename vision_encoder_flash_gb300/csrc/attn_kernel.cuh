@@ -91,6 +91,9 @@ struct Plan {
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   static constexpr int kConvWarps = 16 - 2 - 4 * NQ;
   static constexpr int kConvThreads = kConvWarps * 32;
+  static constexpr uint32_t kRegsSoftmax = 192;
+  static constexpr uint32_t kRegsOther = NQ == 2 ? 64 : 104;
+  static_assert(NQ * kRegsSoftmax + (4 - NQ) * kRegsOther <= 4 * 128, "register split too large");
   static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
 
@@ -169,16 +172,16 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
 }
 
 // f32 slot (rows x d_pad, dense) -> f16 tile rows [row_base, row_base+rows).
+// Thread ct handles 8-column chunk c of rows r, r + dr, ...; when CT is a
+// multiple of the chunks per row, c stays fixed and only r advances.
 template <int CT>
 __device__ __forceinline__ void convert_slot(const float* src, uint8_t* dst, int row_base,
                                              int rows, int d_pad, int ct) {
   const int cpr = d_pad >> 3;
-  const int dr = CT / cpr, dc = CT % cpr;
-  int r = ct / cpr, c = ct % cpr;
-  while (r < rows) {
+  // threads with (c & 4) read their upper half first: the 8 threads of a
+  // shared-memory phase then touch all 32 banks once
+  auto one = [&](int r, int c) {
     const float* s = src + r * d_pad + c * 8;
-    // threads with (c & 4) read their upper half first: the 8 threads of a
-    // shared-memory phase then touch all 32 banks once
     const int sw = (c & 4);
     const float4 x0 = *reinterpret_cast<const float4*>(s + sw);
     const float4 x1 = *reinterpret_cast<const float4*>(s + (4 - sw));
@@ -186,11 +189,22 @@ __device__ __forceinline__ void convert_slot(const float* src, uint8_t* dst, int
     const float4 b = sw ? x0 : x1;
     const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     *reinterpret_cast<uint4*>(dst + f16_chunk_offset(row_base + r, c)) = pack8(x);
-    r += dr;
-    c += dc;
-    if (c >= cpr) {
-      c -= cpr;
-      ++r;
+  };
+  if (CT % cpr == 0) {
+    const int dr = CT / cpr;
+    const int c = ct % cpr;
+    for (int r = ct / cpr; r < rows; r += dr) one(r, c);
+  } else {
+    const int dr = CT / cpr, dc = CT % cpr;
+    int r = ct / cpr, c = ct % cpr;
+    while (r < rows) {
+      one(r, c);
+      r += dr;
+      c += dc;
+      if (c >= cpr) {
+        c -= cpr;
+        ++r;
+      }
     }
   }
 }
@@ -272,118 +286,168 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + P::kOffBar + kTmemSlotOff);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (kTma && lane == 0) {
-      ptx::prefetch_tensormap(&tm_q);
-      ptx::prefetch_tensormap(&tm_k);
-      ptx::prefetch_tensormap(&tm_v);
-      const uint32_t slot_bytes = static_cast<uint32_t>(P::kSlotRows * p.d_pad * 4);
-      int load = 0;
-      bool ok = true;
-      auto issue = [&](const CUtensorMap* tm, int row) {
-        const int slot = load % P::kF32Slots;
-        const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
-        if (!w.wait(bar(kBarF32Empty + slot), (use & 1u) ^ 1u, kSiteProducerSlot)) {
-          ok = false;
-          return;
-        }
-        ptx::mbar_arrive_expect_tx(bar(kBarF32Full + slot), slot_bytes);
-        ptx::tma_load_3d(base_s + P::kOffF32 + slot * kSlotBytes, tm, bar(kBarF32Full + slot), 0,
-                         row, bh);
-        ++load;
-      };
-      for (int t = 0; ok && t < NQ; ++t)
-        for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_q, q_row0 + t * kBM + s * P::kSlotRows);
-      for (int j = 0; ok && j < T; ++j) {
-        for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_k, j * kBN + s * P::kSlotRows);
-        for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_v, j * kBN + s * P::kSlotRows);
-      }
-      // the newest copy into each slot must have landed before exit
-      for (int slot = 0; slot < P::kF32Slots; ++slot) {
-        if (load > slot) {
-          const int uses = (load - 1 - slot) / P::kF32Slots + 1;
-          w.drain(bar(kBarF32Full + slot), static_cast<uint32_t>(uses - 1) & 1u, kSiteDrainTma);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_s = ptx::idesc_f16_f32(kBM, kBN, false);
-      const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
-      const int ksteps = p.d_pad >> 4;
-      auto s_col = [](int t, int j) -> uint32_t {
-        return NQ == 2 ? static_cast<uint32_t>(t) * 128u : static_cast<uint32_t>(j & 1) * 128u;
-      };
-      auto issue_s = [&](int t, int j) {
-        const uint32_t qa = base_s + P::kOffQ + t * P::kTileF16;
-        const uint32_t kb = base_s + P::kOffK + (j & 1) * P::kTileF16;
-        const uint32_t d = tmem + s_col(t, j);
-        for (int ks = 0; ks < ksteps; ++ks) {
-          const uint32_t off = static_cast<uint32_t>((ks >> 2) * (128 * 128) + (ks & 3) * 32);
-          ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
-                      ptx::smem_desc(kb + off, 16, 1024, ptx::kSwizzle128B), idesc_s,
-                      ks > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(bar(kBarSFull + (NQ == 2 ? t : (j & 1))));
-      };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t vb = base_s + P::kOffV + (j & 1) * P::kTileF16;
-        const uint32_t d = tmem + 256u + static_cast<uint32_t>(t) * 128u;
-        const uint32_t a = tmem + s_col(t, j);
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
-                      ptx::smem_desc(vb + ks * 2048, 128 * 128, 1024, ptx::kSwizzle128B),
-                      idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(bar(kBarODone + t));
-      };
-
-      bool ok = w.wait(bar(kBarQFull), 0, kSiteMmaQ) && w.wait(bar(kBarKFull), 0, kSiteMmaK);
-      if (ok) {
-        ptx::tc_fence_after();
-        for (int t = 0; t < NQ; ++t) issue_s(t, 0);
-        ptx::mma_commit(bar(kBarKEmpty));
-      }
-      for (int j = 0; ok && j < T; ++j) {
-        const uint32_t st = static_cast<uint32_t>(j & 1);
-        const uint32_t nst = st ^ 1u;
-        const uint32_t nph = static_cast<uint32_t>((j + 1) >> 1) & 1u;
-        if (NQ == 1) {
-          if (j + 1 < T) {
-            if (!(ok = w.wait(bar(kBarKFull + nst), nph, kSiteMmaK))) break;
-            ptx::tc_fence_after();
-            issue_s(0, j + 1);
-            ptx::mma_commit(bar(kBarKEmpty + nst));
+  // register split: the softmax warpgroups hold a whole 128-column S row in
+  // registers; the other warpgroups need few.  Sum over the four warpgroups
+  // stays within the 4 x 128 registers per thread the block launched with.
+  const bool softmax_wg = warp >= 4 && warp < 4 + 4 * NQ;
+  if (!softmax_wg) {
+    ptx::regs_decrease<P::kRegsOther>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (kTma && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        const uint32_t slot_bytes = static_cast<uint32_t>(P::kSlotRows * p.d_pad * 4);
+        int load = 0;
+        bool ok = true;
+        auto issue = [&](const CUtensorMap* tm, int row) {
+          const int slot = load % P::kF32Slots;
+          const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
+          if (!w.wait(bar(kBarF32Empty + slot), (use & 1u) ^ 1u, kSiteProducerSlot)) {
+            ok = false;
+            return;
           }
-          if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
-          if (!(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
-            break;
+          ptx::mbar_arrive_expect_tx(bar(kBarF32Full + slot), slot_bytes);
+          ptx::tma_load_3d(base_s + P::kOffF32 + slot * kSlotBytes, tm, bar(kBarF32Full + slot), 0,
+                           row, bh);
+          ++load;
+        };
+        for (int t = 0; ok && t < NQ; ++t)
+          for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_q, q_row0 + t * kBM + s * P::kSlotRows);
+        for (int j = 0; ok && j < T; ++j) {
+          for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_k, j * kBN + s * P::kSlotRows);
+          for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_v, j * kBN + s * P::kSlotRows);
+        }
+        // the newest copy into each slot must have landed before exit
+        for (int slot = 0; slot < P::kF32Slots; ++slot) {
+          if (load > slot) {
+            const int uses = (load - 1 - slot) / P::kF32Slots + 1;
+            w.drain(bar(kBarF32Full + slot), static_cast<uint32_t>(uses - 1) & 1u, kSiteDrainTma);
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        const uint32_t idesc_s = ptx::idesc_f16_f32(kBM, kBN, false);
+        const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
+        const int ksteps = p.d_pad >> 4;
+        auto s_col = [](int t, int j) -> uint32_t {
+          return NQ == 2 ? static_cast<uint32_t>(t) * 128u : static_cast<uint32_t>(j & 1) * 128u;
+        };
+        auto issue_s = [&](int t, int j) {
+          const uint32_t qa = base_s + P::kOffQ + t * P::kTileF16;
+          const uint32_t kb = base_s + P::kOffK + (j & 1) * P::kTileF16;
+          const uint32_t d = tmem + s_col(t, j);
+          for (int ks = 0; ks < ksteps; ++ks) {
+            const uint32_t off = static_cast<uint32_t>((ks >> 2) * (128 * 128) + (ks & 3) * 32);
+            ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
+                        ptx::smem_desc(kb + off, 16, 1024, ptx::kSwizzle128B), idesc_s,
+                        ks > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(kBarSFull + (NQ == 2 ? t : (j & 1))));
+        };
+        auto issue_pv = [&](int t, int j) {
+          const uint32_t vb = base_s + P::kOffV + (j & 1) * P::kTileF16;
+          const uint32_t d = tmem + 256u + static_cast<uint32_t>(t) * 128u;
+          const uint32_t a = tmem + s_col(t, j);
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
+                        ptx::smem_desc(vb + ks * 2048, 128 * 128, 1024, ptx::kSwizzle128B),
+                        idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(kBarODone + t));
+        };
+
+        bool ok = w.wait(bar(kBarQFull), 0, kSiteMmaQ) && w.wait(bar(kBarKFull), 0, kSiteMmaK);
+        if (ok) {
           ptx::tc_fence_after();
-          issue_pv(0, j);
-          ptx::mma_commit(bar(kBarVEmpty + st));
-        } else {
-          for (int t = 0; t < NQ; ++t) {
-            if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
-            if (t == 0 &&
-                !(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
+          for (int t = 0; t < NQ; ++t) issue_s(t, 0);
+          ptx::mma_commit(bar(kBarKEmpty));
+        }
+        for (int j = 0; ok && j < T; ++j) {
+          const uint32_t st = static_cast<uint32_t>(j & 1);
+          const uint32_t nst = st ^ 1u;
+          const uint32_t nph = static_cast<uint32_t>((j + 1) >> 1) & 1u;
+          if (NQ == 1) {
+            if (j + 1 < T) {
+              if (!(ok = w.wait(bar(kBarKFull + nst), nph, kSiteMmaK))) break;
+              ptx::tc_fence_after();
+              issue_s(0, j + 1);
+              ptx::mma_commit(bar(kBarKEmpty + nst));
+            }
+            if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
+            if (!(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
               break;
             ptx::tc_fence_after();
-            issue_pv(t, j);
-            if (t == NQ - 1) ptx::mma_commit(bar(kBarVEmpty + st));
-            if (j + 1 < T) {
-              if (t == 0 && !(ok = w.wait(bar(kBarKFull + nst), nph, kSiteMmaK))) break;
+            issue_pv(0, j);
+            ptx::mma_commit(bar(kBarVEmpty + st));
+          } else {
+            for (int t = 0; t < NQ; ++t) {
+              if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
+              if (t == 0 &&
+                  !(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
+                break;
               ptx::tc_fence_after();
-              issue_s(t, j + 1);
-              if (t == NQ - 1) ptx::mma_commit(bar(kBarKEmpty + nst));
+              issue_pv(t, j);
+              if (t == NQ - 1) ptx::mma_commit(bar(kBarVEmpty + st));
+              if (j + 1 < T) {
+                if (t == 0 && !(ok = w.wait(bar(kBarKFull + nst), nph, kSiteMmaK))) break;
+                ptx::tc_fence_after();
+                issue_s(t, j + 1);
+                if (t == NQ - 1) ptx::mma_commit(bar(kBarKEmpty + nst));
+              }
             }
           }
         }
+        ptx::mma_commit(bar(kBarMmaDone));
       }
-      ptx::mma_commit(bar(kBarMmaDone));
+    } else {
+      // ------------------------------------------------------------ converters
+      const int ct = (warp < 4 ? warp - 2 : warp - 2 - 4 * NQ) * 32 + lane;
+      constexpr int CT = P::kConvThreads;
+      const size_t head_off = static_cast<size_t>(bh) * N * p.head_dim;
+      int load = 0;
+      bool ok = true;
+      // one 128-row tile (f32 source rows tile_row0..) into the f16 tile at dst
+      auto tile = [&](const float* g, int tile_row0, uint8_t* dst) {
+        if (kTma) {
+          for (int s = 0; s < P::kSubs; ++s) {
+            const int slot = load % P::kF32Slots;
+            const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
+            if (!(ok = w.wait(bar(kBarF32Full + slot), use & 1u, kSiteConvSlot))) return;
+            convert_slot<CT>(reinterpret_cast<const float*>(base + P::kOffF32 + slot * kSlotBytes),
+                             dst, s * P::kSlotRows, P::kSlotRows, p.d_pad, ct);
+            ptx::mbar_arrive(bar(kBarF32Empty + slot));
+            ++load;
+          }
+        } else {
+          convert_global<CT>(g + head_off, tile_row0, N - tile_row0, p.head_dim, dst, p.d_pad, ct);
+        }
+      };
+      for (int t = 0; ok && t < NQ; ++t) tile(p.q, q_row0 + t * kBM, base + P::kOffQ + t * P::kTileF16);
+      if (ok) {
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar(kBarQFull));
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u;
+        if (!(ok = w.wait(bar(kBarKEmpty + st), ph, kSiteConvKStage))) break;
+        tile(p.k, j * kBN, base + P::kOffK + st * P::kTileF16);
+        if (!ok) break;
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar(kBarKFull + st));
+        if (!(ok = w.wait(bar(kBarVEmpty + st), ph, kSiteConvVStage))) break;
+        tile(p.v, j * kBN, base + P::kOffV + st * P::kTileF16);
+        if (!ok) break;
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar(kBarVFull + st));
+      }
     }
-  } else if (warp >= 4 && warp < 4 + 4 * NQ) {
+  } else {
+    ptx::regs_increase<P::kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -399,46 +463,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = w.wait_warp(bar(kBarSFull + buf), par, kSiteSoftS))) break;
       ptx::tc_fence_after();
       const uint32_t s_addr = tmem + lane_addr + static_cast<uint32_t>(buf) * 128u;
-      const int valid = min(kBN, N - j * kBN);
+      const int valid = N - j * kBN;
 
-      float mx = -INFINITY;
+      // the whole S row (128 columns) into registers, one wait
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(s_addr + c * 32, r[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld_dep(r[c]);
+      if (valid < kBN) {  // ragged last key tile only: keys >= n_patches score -inf
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= valid) r[c][i] = 0xff800000u;
+      }
+      float mc[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, r);
-        ptx::tmem_wait_ld();
+        float a = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float s = (c * 32 + i < valid) ? __uint_as_float(r[i]) : -INFINITY;
-          mx = fmaxf(mx, s);
-        }
+        for (int i = 0; i < 32; i += 2)
+          a = ptx::max3(a, __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+        mc[c] = a;
       }
-      const float mt = mx * kLog2e;
+      const float mt = ptx::max3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * kLog2e;
       const bool need = mt > m_ref + kRescaleLog2;
       const float m_new = need ? mt : m_ref;
       const float alpha = ptx::ex2_approx(m_ref - m_new);  // 0 on the first tile, 1 if kept
-      l *= alpha;
       m_ref = m_new;
 
+      // p = 2^(s*log2e - m_ref); P (f16 pairs) overwrites S columns [0, 64)
+      const float2 scale = make_float2(kLog2e, kLog2e);
+      const float2 shift = make_float2(-m_ref, -m_ref);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(s_addr + c * 32, r);
-        ptx::tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int col = c * 32 + 2 * i;
-          const float s0 = col < valid ? __uint_as_float(r[2 * i]) : -INFINITY;
-          const float s1 = col + 1 < valid ? __uint_as_float(r[2 * i + 1]) : -INFINITY;
-          const float p0 = ptx::ex2_approx(fmaf(s0, kLog2e, -m_ref));
-          const float p1 = ptx::ex2_approx(fmaf(s1, kLog2e, -m_ref));
-          l += p0 + p1;
-          pk[i] = ptx::pack_half2(p0, p1);
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), scale,
+              shift);
+          const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
+          pk[i] = ptx::pack_half2(pp.x, pp.y);
         }
-        // P (f16 pairs) overwrites S columns [16c, 16c+16), all already read
         ptx::tmem_st_32x32b_x16(s_addr + c * 16, pk);
       }
+      const float2 s01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 s23 = __fadd2_rn(acc[2], acc[3]);
+      l = fmaf(l, alpha, (s01.x + s01.y) + (s23.x + s23.y));
 
       if (j > 0) {
         if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(j - 1) & 1u, kSiteSoftO)))
@@ -448,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < (p.d_pad >> 4); ++c) {
             uint32_t y[16];
             ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
-            ptx::tmem_wait_ld();
+            ptx::tmem_wait_ld_dep16(y);
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
             ptx::tmem_st_32x32b_x16(o_addr + c * 16, y);
@@ -468,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < (p.d_pad >> 4); ++c) {
         uint32_t y[16];
         ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
-        ptx::tmem_wait_ld();
+        ptx::tmem_wait_ld_dep16(y);
         if (row < N) {
           if (p.vec_out) {
 #pragma unroll
@@ -492,48 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    }
-  } else {
-    // ------------------------------------------------------------ converters
-    const int ct = (warp < 4 ? warp - 2 : warp - 2 - 4 * NQ) * 32 + lane;
-    constexpr int CT = P::kConvThreads;
-    const size_t head_off = static_cast<size_t>(bh) * N * p.head_dim;
-    int load = 0;
-    bool ok = true;
-    // one 128-row tile (f32 source rows tile_row0..) into the f16 tile at dst
-    auto tile = [&](const float* g, int tile_row0, uint8_t* dst) {
-      if (kTma) {
-        for (int s = 0; s < P::kSubs; ++s) {
-          const int slot = load % P::kF32Slots;
-          const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
-          if (!(ok = w.wait(bar(kBarF32Full + slot), use & 1u, kSiteConvSlot))) return;
-          convert_slot<CT>(reinterpret_cast<const float*>(base + P::kOffF32 + slot * kSlotBytes),
-                           dst, s * P::kSlotRows, P::kSlotRows, p.d_pad, ct);
-          ptx::mbar_arrive(bar(kBarF32Empty + slot));
-          ++load;
-        }
-      } else {
-        convert_global<CT>(g + head_off, tile_row0, N - tile_row0, p.head_dim, dst, p.d_pad, ct);
-      }
-    };
-    for (int t = 0; ok && t < NQ; ++t) tile(p.q, q_row0 + t * kBM, base + P::kOffQ + t * P::kTileF16);
-    if (ok) {
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(bar(kBarQFull));
-    }
-    for (int j = 0; ok && j < T; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u;
-      if (!(ok = w.wait(bar(kBarKEmpty + st), ph, kSiteConvKStage))) break;
-      tile(p.k, j * kBN, base + P::kOffK + st * P::kTileF16);
-      if (!ok) break;
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(bar(kBarKFull + st));
-      if (!(ok = w.wait(bar(kBarVEmpty + st), ph, kSiteConvVStage))) break;
-      tile(p.v, j * kBN, base + P::kOffV + st * P::kTileF16);
-      if (!ok) break;
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(bar(kBarVFull + st));
     }
   }
 
