@@ -14,12 +14,18 @@
 //   * "converter" warps turn each f32 tile into f16 in the 128-byte-swizzled
 //     layout the tensor core reads (the shader's f32 -> f16 staging);
 //   * warp 1 issues tcgen05.mma: S = Q K^T (f32 in TMEM), then O += P V with
-//     P taken from TMEM (it overwrites S in place) and V from shared memory;
+//     P taken from TMEM and V from shared memory.  S and P have separate
+//     TMEM columns, so the next S = Q K^T is issued as soon as the softmax
+//     has copied the current S into registers and runs while the softmax
+//     computes its exponentials;
 //   * one warpgroup per query tile runs the online softmax: thread = query
 //     row, so the row max and row sum need no shuffles; exp is exp2 with
 //     log2(e) folded into one FMA; O is rescaled in TMEM only when the
 //     row max grew by more than 2^8 (exact after the final 1/l);
 //   * the same warpgroup divides by l and stores its rows of out.
+// TMEM columns (512): S buffers [0,128) and [128,256); with two query tiles
+// P0, P1 at 256, 320 and O0, O1 at 384, 448 (head_dim <= 64); with one query
+// tile P at 256 and O at 320 (head_dim <= 128).
 // Every wait is bounded: on timeout the block records the wait site in
 // g_vattn_status, raises a shared abort flag so the other roles leave their
 // loops, drains its own TMA copies and MMAs, frees TMEM and exits.
@@ -56,6 +62,7 @@ enum WaitSite : uint32_t {
   kSiteEpilogue = 11,
   kSiteDrainTma = 12,
   kSiteDrainMma = 13,
+  kSiteMmaSFree = 14,
 };
 constexpr uint32_t kStatusTimeout = 0x100u;
 
@@ -91,29 +98,36 @@ struct Plan {
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   static constexpr int kConvWarps = 16 - 2 - 4 * NQ;
   static constexpr int kConvThreads = kConvWarps * 32;
-  static constexpr uint32_t kRegsSoftmax = 192;
-  static constexpr uint32_t kRegsOther = NQ == 2 ? 64 : 104;
+  static constexpr uint32_t kRegsSoftmax = 184;
+  static constexpr uint32_t kRegsOther = NQ == 2 ? 72 : 104;
+  // TMEM columns
+  static constexpr uint32_t kColP = 256;
+  static constexpr uint32_t kColO = NQ == 2 ? 384 : 320;
+  static constexpr uint32_t kColStride = 64;  // between the tiles' P (and O) blocks
   static_assert(NQ * kRegsSoftmax + (4 - NQ) * kRegsOther <= 4 * 128, "register split too large");
   static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
+  static_assert(NQ == 1 || NKB == 1, "two query tiles need head_dim <= 64");
 };
 
 // mbarrier indices inside the barrier block.
 enum Bar : int {
-  kBarF32Full = 0,    // [4] TMA landed in slot
-  kBarF32Empty = 4,   // [4] converters done reading slot
-  kBarKFull = 8,      // [2] f16 K stage written
-  kBarKEmpty = 10,    // [2] S MMAs done with K stage
-  kBarVFull = 12,     // [2] f16 V stage written
-  kBarVEmpty = 14,    // [2] P.V MMAs done with V stage
-  kBarQFull = 16,     // f16 Q tiles written
-  kBarSFull = 17,     // [2] S tile complete in TMEM
-  kBarPFull = 19,     // [2] P written to TMEM and O rescaled (per query tile)
-  kBarODone = 21,     // [2] P.V complete (per query tile)
-  kBarMmaDone = 23,   // every MMA of the block complete
-  kNumBars = 24,
+  kBarF32Full = 0,    // [4] TMA landed in slot                      (count 1 + tx)
+  kBarF32Empty = 4,   // [4] converters done reading slot            (one per converter warp)
+  kBarKFull = 8,      // [2] f16 K stage written                      (one per converter warp)
+  kBarKEmpty = 10,    // [2] S MMAs done with K stage                (commit)
+  kBarVFull = 12,     // [2] f16 V stage written                      (one per converter warp)
+  kBarVEmpty = 14,    // [2] P.V MMAs done with V stage              (commit)
+  kBarQFull = 16,     // f16 Q tiles written                          (one per converter warp)
+  kBarSFull = 17,     // [2] S buffer complete in TMEM               (commit)
+  kBarSFree = 19,     // [2] S buffer copied to registers            (one per softmax warp)
+  kBarPFull = 21,     // [2] P written, O rescaled (per query tile)  (one per softmax warp)
+  kBarODone = 23,     // [2] P.V complete (per query tile)           (commit)
+  kBarMmaDone = 25,   // every MMA of the block complete             (commit)
+  kNumBars = 26,
 };
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
 constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
+static_assert(kAbortOff + 4 <= 256, "barrier block overflow");
 
 struct Waiter {
   volatile uint32_t* abort_flag;
@@ -156,6 +170,13 @@ struct Waiter {
   }
 };
 
+// One arrival per warp: the lanes' earlier memory operations are ordered
+// before lane 0's (release) arrive by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
+}
+
 // f16 tile address of element chunk (row R, 8-column chunk c): block c/8 of
 // 128 rows x 128 bytes; 16-byte chunk (c%8) ^ (R%8) within the row.
 __device__ __forceinline__ uint32_t f16_chunk_offset(int R, int c) {
@@ -172,38 +193,44 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
 }
 
 // f32 slot (rows x d_pad, dense) -> f16 tile rows [row_base, row_base+rows).
-// Thread ct handles 8-column chunk c of rows r, r + dr, ...; when CT is a
-// multiple of the chunks per row, c stays fixed and only r advances.
+// The first (CT / cpr) * cpr converter threads take part (cpr = 8-column
+// chunks per row): thread ct keeps chunk column ct % cpr and walks rows
+// ct / cpr, + CT / cpr, ...  Loads are issued kBatch chunks ahead of their
+// conversion so the shared-memory latencies overlap.
 template <int CT>
-__device__ __forceinline__ void convert_slot(const float* src, uint8_t* dst, int row_base,
-                                             int rows, int d_pad, int ct) {
+__device__ __forceinline__ void convert_slot(const float* __restrict__ src,
+                                             uint8_t* __restrict__ dst, int row_base, int rows,
+                                             int d_pad, int ct) {
+  constexpr int kBatch = 3;
   const int cpr = d_pad >> 3;
+  const int dr = CT / cpr;
+  if (ct >= dr * cpr) return;
+  const int c = ct % cpr;
   // threads with (c & 4) read their upper half first: the 8 threads of a
   // shared-memory phase then touch all 32 banks once
-  auto one = [&](int r, int c) {
-    const float* s = src + r * d_pad + c * 8;
-    const int sw = (c & 4);
-    const float4 x0 = *reinterpret_cast<const float4*>(s + sw);
-    const float4 x1 = *reinterpret_cast<const float4*>(s + (4 - sw));
-    const float4 a = sw ? x1 : x0;
-    const float4 b = sw ? x0 : x1;
-    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    *reinterpret_cast<uint4*>(dst + f16_chunk_offset(row_base + r, c)) = pack8(x);
-  };
-  if (CT % cpr == 0) {
-    const int dr = CT / cpr;
-    const int c = ct % cpr;
-    for (int r = ct / cpr; r < rows; r += dr) one(r, c);
-  } else {
-    const int dr = CT / cpr, dc = CT % cpr;
-    int r = ct / cpr, c = ct % cpr;
-    while (r < rows) {
-      one(r, c);
-      r += dr;
-      c += dc;
-      if (c >= cpr) {
-        c -= cpr;
-        ++r;
+  const int sw = c & 4;
+  const float* s0 = src + c * 8;
+  uint8_t* const d0 = dst + (c >> 3) * (128 * 128);
+  const int cc = c & 7;
+  for (int r0 = ct / cpr; r0 < rows; r0 += kBatch * dr) {
+    float4 lo[kBatch], hi[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int r = r0 + u * dr;
+      if (r < rows) {
+        const float* s = s0 + r * d_pad;
+        const float4 x0 = *reinterpret_cast<const float4*>(s + sw);
+        const float4 x1 = *reinterpret_cast<const float4*>(s + (4 - sw));
+        lo[u] = sw ? x1 : x0;
+        hi[u] = sw ? x0 : x1;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int R = row_base + r0 + u * dr;
+      if (r0 + u * dr < rows) {
+        const float x[8] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w, hi[u].x, hi[u].y, hi[u].z, hi[u].w};
+        *reinterpret_cast<uint4*>(d0 + R * 128 + ((cc ^ (R & 7)) << 4)) = pack8(x);
       }
     }
   }
@@ -258,21 +285,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = p.n_patches;
   const int T = p.n_ktiles;
 
+  // S buffer of query tile t for key tile j, and the phase of its barriers
+  auto sbuf = [](int t, int j) -> int { return NQ == 2 ? t : (j & 1); };
+  auto sphase = [](int j) -> uint32_t {
+    return NQ == 2 ? (static_cast<uint32_t>(j) & 1u) : (static_cast<uint32_t>(j >> 1) & 1u);
+  };
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < P::kF32Slots; ++i) {
       ptx::mbar_init(bar(kBarF32Full + i), 1);
-      ptx::mbar_init(bar(kBarF32Empty + i), P::kConvThreads);
+      ptx::mbar_init(bar(kBarF32Empty + i), P::kConvWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(bar(kBarKFull + i), P::kConvThreads);
+      ptx::mbar_init(bar(kBarKFull + i), P::kConvWarps);
       ptx::mbar_init(bar(kBarKEmpty + i), 1);
-      ptx::mbar_init(bar(kBarVFull + i), P::kConvThreads);
+      ptx::mbar_init(bar(kBarVFull + i), P::kConvWarps);
       ptx::mbar_init(bar(kBarVEmpty + i), 1);
       ptx::mbar_init(bar(kBarSFull + i), 1);
-      ptx::mbar_init(bar(kBarPFull + i), 128);
+      ptx::mbar_init(bar(kBarSFree + i), 4);
+      ptx::mbar_init(bar(kBarPFull + i), 4);
       ptx::mbar_init(bar(kBarODone + i), 1);
     }
-    ptx::mbar_init(bar(kBarQFull), P::kConvThreads);
+    ptx::mbar_init(bar(kBarQFull), P::kConvWarps);
     ptx::mbar_init(bar(kBarMmaDone), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -293,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!softmax_wg) {
     ptx::regs_decrease<P::kRegsOther>();
     if (warp == 0) {
-      // ------------------------------------------------------------ producer
+      // ---------------------------------------------------------- producer
       if (kTma && lane == 0) {
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
@@ -309,12 +343,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             return;
           }
           ptx::mbar_arrive_expect_tx(bar(kBarF32Full + slot), slot_bytes);
-          ptx::tma_load_3d(base_s + P::kOffF32 + slot * kSlotBytes, tm, bar(kBarF32Full + slot), 0,
-                           row, bh);
+          ptx::tma_load_3d(base_s + P::kOffF32 + slot * kSlotBytes, tm, bar(kBarF32Full + slot),
+                           0, row, bh);
           ++load;
         };
         for (int t = 0; ok && t < NQ; ++t)
-          for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_q, q_row0 + t * kBM + s * P::kSlotRows);
+          for (int s = 0; ok && s < P::kSubs; ++s)
+            issue(&tm_q, q_row0 + t * kBM + s * P::kSlotRows);
         for (int j = 0; ok && j < T; ++j) {
           for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_k, j * kBN + s * P::kSlotRows);
           for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_v, j * kBN + s * P::kSlotRows);
@@ -323,35 +358,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int slot = 0; slot < P::kF32Slots; ++slot) {
           if (load > slot) {
             const int uses = (load - 1 - slot) / P::kF32Slots + 1;
-            w.drain(bar(kBarF32Full + slot), static_cast<uint32_t>(uses - 1) & 1u, kSiteDrainTma);
+            w.drain(bar(kBarF32Full + slot), static_cast<uint32_t>(uses - 1) & 1u,
+                    kSiteDrainTma);
           }
         }
       }
     } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
+      // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
         const uint32_t idesc_s = ptx::idesc_f16_f32(kBM, kBN, false);
         const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
         const int ksteps = p.d_pad >> 4;
-        auto s_col = [](int t, int j) -> uint32_t {
-          return NQ == 2 ? static_cast<uint32_t>(t) * 128u : static_cast<uint32_t>(j & 1) * 128u;
-        };
+        // S(t, j) = Q_t K_j^T into S buffer sbuf(t, j)
         auto issue_s = [&](int t, int j) {
           const uint32_t qa = base_s + P::kOffQ + t * P::kTileF16;
           const uint32_t kb = base_s + P::kOffK + (j & 1) * P::kTileF16;
-          const uint32_t d = tmem + s_col(t, j);
+          const uint32_t d = tmem + static_cast<uint32_t>(sbuf(t, j)) * 128u;
           for (int ks = 0; ks < ksteps; ++ks) {
             const uint32_t off = static_cast<uint32_t>((ks >> 2) * (128 * 128) + (ks & 3) * 32);
             ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
                         ptx::smem_desc(kb + off, 16, 1024, ptx::kSwizzle128B), idesc_s,
                         ks > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(bar(kBarSFull + (NQ == 2 ? t : (j & 1))));
+          ptx::mma_commit(bar(kBarSFull + sbuf(t, j)));
         };
+        // O_t += P_t V_j
         auto issue_pv = [&](int t, int j) {
           const uint32_t vb = base_s + P::kOffV + (j & 1) * P::kTileF16;
-          const uint32_t d = tmem + 256u + static_cast<uint32_t>(t) * 128u;
-          const uint32_t a = tmem + s_col(t, j);
+          const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
+          const uint32_t a = tmem + P::kColP + static_cast<uint32_t>(t) * P::kColStride;
           for (int ks = 0; ks < kBN / 16; ++ks) {
             ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
                         ptx::smem_desc(vb + ks * 2048, 128 * 128, 1024, ptx::kSwizzle128B),
@@ -367,44 +402,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit(bar(kBarKEmpty));
         }
         for (int j = 0; ok && j < T; ++j) {
-          const uint32_t st = static_cast<uint32_t>(j & 1);
-          const uint32_t nst = st ^ 1u;
-          const uint32_t nph = static_cast<uint32_t>((j + 1) >> 1) & 1u;
-          if (NQ == 1) {
-            if (j + 1 < T) {
-              if (!(ok = w.wait(bar(kBarKFull + nst), nph, kSiteMmaK))) break;
-              ptx::tc_fence_after();
-              issue_s(0, j + 1);
-              ptx::mma_commit(bar(kBarKEmpty + nst));
-            }
-            if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
-            if (!(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
+          const int st = j & 1;
+          if (j + 1 < T) {
+            // next S as early as possible: it only needs K_{j+1} and the
+            // softmax to have copied the previous contents of its buffer
+            const int nst = st ^ 1;
+            if (!(ok = w.wait(bar(kBarKFull + nst), static_cast<uint32_t>((j + 1) >> 1) & 1u,
+                              kSiteMmaK)))
               break;
-            ptx::tc_fence_after();
-            issue_pv(0, j);
-            ptx::mma_commit(bar(kBarVEmpty + st));
-          } else {
-            for (int t = 0; t < NQ; ++t) {
-              if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
-              if (t == 0 &&
-                  !(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
+            for (int t = 0; ok && t < NQ; ++t) {
+              const int prev = NQ == 2 ? j : j - 1;  // last key tile that used this buffer
+              if (prev >= 0 && !(ok = w.wait(bar(kBarSFree + sbuf(t, j + 1)), sphase(prev),
+                                             kSiteMmaSFree)))
                 break;
               ptx::tc_fence_after();
-              issue_pv(t, j);
-              if (t == NQ - 1) ptx::mma_commit(bar(kBarVEmpty + st));
-              if (j + 1 < T) {
-                if (t == 0 && !(ok = w.wait(bar(kBarKFull + nst), nph, kSiteMmaK))) break;
-                ptx::tc_fence_after();
-                issue_s(t, j + 1);
-                if (t == NQ - 1) ptx::mma_commit(bar(kBarKEmpty + nst));
-              }
+              issue_s(t, j + 1);
             }
+            if (!ok) break;
+            ptx::mma_commit(bar(kBarKEmpty + nst));
           }
+          if (!(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
+            break;
+          for (int t = 0; ok && t < NQ; ++t) {
+            if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
+            ptx::tc_fence_after();
+            issue_pv(t, j);
+          }
+          if (!ok) break;
+          ptx::mma_commit(bar(kBarVEmpty + st));
         }
         ptx::mma_commit(bar(kBarMmaDone));
       }
     } else {
-      // ------------------------------------------------------------ converters
+      // ---------------------------------------------------------- converters
+      // (warp-uniform waits: every converter lane reaches each warp_arrive)
       const int ct = (warp < 4 ? warp - 2 : warp - 2 - 4 * NQ) * 32 + lane;
       constexpr int CT = P::kConvThreads;
       const size_t head_off = static_cast<size_t>(bh) * N * p.head_dim;
@@ -416,34 +447,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < P::kSubs; ++s) {
             const int slot = load % P::kF32Slots;
             const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
-            if (!(ok = w.wait(bar(kBarF32Full + slot), use & 1u, kSiteConvSlot))) return;
-            convert_slot<CT>(reinterpret_cast<const float*>(base + P::kOffF32 + slot * kSlotBytes),
-                             dst, s * P::kSlotRows, P::kSlotRows, p.d_pad, ct);
-            ptx::mbar_arrive(bar(kBarF32Empty + slot));
+            if (!(ok = w.wait_warp(bar(kBarF32Full + slot), use & 1u, kSiteConvSlot))) return;
+            convert_slot<CT>(
+                reinterpret_cast<const float*>(base + P::kOffF32 + slot * kSlotBytes), dst,
+                s * P::kSlotRows, P::kSlotRows, p.d_pad, ct);
+            warp_arrive(bar(kBarF32Empty + slot));
             ++load;
           }
         } else {
-          convert_global<CT>(g + head_off, tile_row0, N - tile_row0, p.head_dim, dst, p.d_pad, ct);
+          convert_global<CT>(g + head_off, tile_row0, N - tile_row0, p.head_dim, dst, p.d_pad,
+                             ct);
         }
       };
-      for (int t = 0; ok && t < NQ; ++t) tile(p.q, q_row0 + t * kBM, base + P::kOffQ + t * P::kTileF16);
+      for (int t = 0; ok && t < NQ; ++t)
+        tile(p.q, q_row0 + t * kBM, base + P::kOffQ + t * P::kTileF16);
       if (ok) {
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(bar(kBarQFull));
+        warp_arrive(bar(kBarQFull));
       }
       for (int j = 0; ok && j < T; ++j) {
         const int st = j & 1;
         const uint32_t ph = (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u;
-        if (!(ok = w.wait(bar(kBarKEmpty + st), ph, kSiteConvKStage))) break;
+        if (!(ok = w.wait_warp(bar(kBarKEmpty + st), ph, kSiteConvKStage))) break;
         tile(p.k, j * kBN, base + P::kOffK + st * P::kTileF16);
         if (!ok) break;
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(bar(kBarKFull + st));
-        if (!(ok = w.wait(bar(kBarVEmpty + st), ph, kSiteConvVStage))) break;
+        warp_arrive(bar(kBarKFull + st));
+        if (!(ok = w.wait_warp(bar(kBarVEmpty + st), ph, kSiteConvVStage))) break;
         tile(p.v, j * kBN, base + P::kOffV + st * P::kTileF16);
         if (!ok) break;
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(bar(kBarVFull + st));
+        warp_arrive(bar(kBarVFull + st));
       }
     }
   } else {
@@ -452,25 +486,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t o_addr = tmem + lane_addr + 256u + static_cast<uint32_t>(t) * 128u;
+    const uint32_t p_addr = tmem + lane_addr + P::kColP + static_cast<uint32_t>(t) * P::kColStride;
+    const uint32_t o_addr = tmem + lane_addr + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
     float m_ref = -INFINITY;  // running max in log2 units (may lag the true max by < 8)
     float l = 0.0f;           // running sum of exp2(s*log2e - m_ref)
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      const int buf = NQ == 2 ? t : (j & 1);
-      const uint32_t par = NQ == 2 ? (static_cast<uint32_t>(j) & 1u)
-                                   : (static_cast<uint32_t>(j >> 1) & 1u);
-      if (!(ok = w.wait_warp(bar(kBarSFull + buf), par, kSiteSoftS))) break;
+      const int buf = sbuf(t, j);
+      if (!(ok = w.wait_warp(bar(kBarSFull + buf), sphase(j), kSiteSoftS))) break;
       ptx::tc_fence_after();
       const uint32_t s_addr = tmem + lane_addr + static_cast<uint32_t>(buf) * 128u;
       const int valid = N - j * kBN;
 
-      // the whole S row (128 columns) into registers, one wait
+      // the whole S row (128 columns) into registers, one wait; then the
+      // buffer is released for the next S = Q K^T
       uint32_t r[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(s_addr + c * 32, r[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld_dep(r[c]);
+      ptx::tc_fence_before();
+      warp_arrive(bar(kBarSFree + buf));
+
       if (valid < kBN) {  // ragged last key tile only: keys >= n_patches score -inf
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -493,7 +530,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = ptx::ex2_approx(m_ref - m_new);  // 0 on the first tile, 1 if kept
       m_ref = m_new;
 
-      // p = 2^(s*log2e - m_ref); P (f16 pairs) overwrites S columns [0, 64)
+      if (j > 0) {
+        // P.V of the previous key tile has finished: P buffer free, O final
+        if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(j - 1) & 1u,
+                               kSiteSoftO)))
+          break;
+        ptx::tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          for (int c = 0; c < (p.d_pad >> 4); ++c) {
+            uint32_t y[16];
+            ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
+            ptx::tmem_wait_ld_dep16(y);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
+            ptx::tmem_st_32x32b_x16(o_addr + c * 16, y);
+          }
+        }
+      }
+
+      // p = 2^(s*log2e - m_ref), stored as f16 pairs in this tile's P buffer
       const float2 scale = make_float2(kLog2e, kLog2e);
       const float2 shift = make_float2(-m_ref, -m_ref);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -510,30 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
           pk[i] = ptx::pack_half2(pp.x, pp.y);
         }
-        ptx::tmem_st_32x32b_x16(s_addr + c * 16, pk);
+        ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk);
       }
       const float2 s01 = __fadd2_rn(acc[0], acc[1]);
       const float2 s23 = __fadd2_rn(acc[2], acc[3]);
       l = fmaf(l, alpha, (s01.x + s01.y) + (s23.x + s23.y));
 
-      if (j > 0) {
-        if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(j - 1) & 1u, kSiteSoftO)))
-          break;
-        if (__any_sync(0xffffffffu, need)) {
-          ptx::tc_fence_after();
-          for (int c = 0; c < (p.d_pad >> 4); ++c) {
-            uint32_t y[16];
-            ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
-            ptx::tmem_wait_ld_dep16(y);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
-            ptx::tmem_st_32x32b_x16(o_addr + c * 16, y);
-          }
-        }
-      }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(kBarPFull + t));
+      warp_arrive(bar(kBarPFull + t));
     }
     if (ok && w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(T - 1) & 1u, kSiteEpilogue)) {
       ptx::tc_fence_after();

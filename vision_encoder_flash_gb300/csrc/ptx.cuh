@@ -42,16 +42,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// Non-blocking probe of a phase: true once the phase of parity `parity`
-// has completed.
+// Probe of a phase: true once the phase of parity `parity` has completed.
+// The thread may be suspended in hardware for up to kSuspendHintNs while
+// the phase is pending, so a waiting warp does not spin on issue slots.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return done != 0;
 }
