@@ -53,6 +53,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: the work of all ranks over the slowest rank's time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -260,13 +275,6 @@ def run_vattn(args, workload):
         if pg is not None:
             pg.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if pg is None:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        return float(t.item())
-
     vef.load_library()
     q, k, v = make_inputs(workload.batch, workload.n_heads, workload.n_patches, workload.head_dim,
                           workload.seed + 1000 * rank, workload.peaked)
@@ -310,10 +318,10 @@ def run_vattn(args, workload):
     sampler.stop()
     clocks = sampler.summary(host_t0, host_t1)
 
-    ms_per_step = max_over_ranks(total_ms / args.steps)
-    kernel_ms = max_over_ranks(sum(launch_ms) / len(launch_ms))
+    ms_per_step = max_over_ranks(total_ms / args.steps, pg, dev)
+    kernel_ms = max_over_ranks(sum(launch_ms) / len(launch_ms), pg, dev)
     flops = float(workload.flops)
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    value = weak_scaling_value(flops, world, ms_per_step)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
 
     pk, pk_src = peaks()
@@ -329,8 +337,8 @@ def run_vattn(args, workload):
     t = time.perf_counter()
     for _ in range(e2e_steps):
         vef.forward(qh, kh, vh, out=oh)  # H2D copies, kernel, D2H copy, stream sync
-    e2e_s = max_over_ranks((time.perf_counter() - t) / e2e_steps)
-    e2e_value = flops * world / e2e_s / 1e12
+    e2e_s = max_over_ranks((time.perf_counter() - t) / e2e_steps, pg, dev)
+    e2e_value = weak_scaling_value(flops, world, e2e_s * 1e3)
     h2d = 3 * q.nbytes
     d2h = oh.numel() * 4
 

@@ -98,6 +98,19 @@ def test_small_shapes(torch_dev, d, n):
     assert_parity(got, oracle.forward(q, k, v), f"D={d} N={n}", rel_l2=2 * MAX_REL_L2)
 
 
+# head_dim <= 64 with more than two query tiles: several thread blocks per
+# head, ragged last block
+PAIR = [(d, n) for d in (8, 20, 32, 48, 60, 64) for n in (257, 511, 512, 513, 1025)]
+
+
+@pytest.mark.parametrize("d,n", PAIR)
+def test_pair_shapes(torch_dev, d, n):
+    q, k, v = make_inputs(1, 3, n, d, seed=3000 + 11 * d + n)
+    got = run_gpu(torch_dev, q, k, v)
+    assert_kernel_arithmetic(got, q, k, v, what=f"pair D={d} N={n}")
+    assert_parity(got, oracle.forward(q, k, v), f"pair D={d} N={n}", rel_l2=2 * MAX_REL_L2)
+
+
 @pytest.mark.parametrize("idx", [1, 2, 3, 4])
 def test_workload_full(torch_dev, idx):
     q, k, v = workload_inputs(idx)
