@@ -39,7 +39,8 @@ if ROOT not in sys.path:
 METRIC = "attention TFLOP/s (4·B·H·N²·D) on 1 GB300; % of dense f16 tensor peak"
 KERNEL_SOURCES = ["vision_encoder_flash_gb300/csrc/attn_kernel.cuh",
                   "vision_encoder_flash_gb300/csrc/ptx.cuh",
-                  "vision_encoder_flash_gb300/csrc/vattn_api.cu"]
+                  "vision_encoder_flash_gb300/csrc/vattn_api.cu",
+                  "vision_encoder_flash_gb300/csrc/stage_kernel.cuh"]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "vattn_fwd_kernel_b8_h16_n2304_d64.md")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 F16_OVER_BF16_NOMINAL = 1.0  # 2.25 PFLOP/s dense for both on GB300

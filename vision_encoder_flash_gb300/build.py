@@ -15,7 +15,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "vattn_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "attn_kernel.cuh"), os.path.join(CSRC, "ptx.cuh"),
+DEPS = SOURCES + [os.path.join(CSRC, "attn_kernel.cuh"), os.path.join(CSRC, "stage_kernel.cuh"),
+                  os.path.join(CSRC, "ptx.cuh"),
                   os.path.join(ROOT, "include", "vattn.h")]
 LIB = os.path.join(PKG, "libvattn.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

@@ -3,16 +3,17 @@
 // Computes, per (batch*head) bh and query row i,
 //     out[bh, i, :] = sum_j softmax_j(q[bh,i,:] . k[bh,j,:]) v[bh, j, :]
 // as in the WGSL shader "vision_attention_flash_sub_hpd_f16.wgsl"
-// (rullama 0.1.0): q/k/v staged to f16, scores and P.V accumulated in f32,
+// (rullama 0.1.0): q/k/v rounded to f16, scores and P.V accumulated in f32,
 // f32 online softmax with running (m, l, o), no 1/sqrt(head_dim) factor.
 //
+// Inputs are the f16 copies written by vattn_stage_kernel (stage_kernel.cuh):
+// [B*H, N, d_pad] f16, d_pad = head_dim rounded up to 16, zero padding.
 // The shader's design (8 queries x 32 keys per 64-thread workgroup, scalar
 // dot products, subgroup reductions) is replaced by a GB300 one:
 //   * one thread block = one bh and NQ query tiles of 128 rows;
-//   * warp 0 streams f32 Q/K/V tiles into a ring of shared-memory slots
-//     with TMA (cp.async.bulk.tensor), out-of-range rows/columns read as 0;
-//   * "converter" warps turn each f32 tile into f16 in the 128-byte-swizzled
-//     layout the tensor core reads (the shader's f32 -> f16 staging);
+//   * warp 0 streams the f16 Q, K and V tiles with TMA
+//     (cp.async.bulk.tensor, 128-byte swizzle) straight into the layout the
+//     tensor core reads; rows past n_patches read as zero;
 //   * warp 1 issues tcgen05.mma: S = Q K^T (f32 in TMEM), then O += P V with
 //     P taken from TMEM and V from shared memory.  S and P have separate
 //     TMEM columns, so the next S = Q K^T is issued as soon as the softmax
@@ -22,7 +23,7 @@
 //     row, so the row max and row sum need no shuffles; exp is exp2 with
 //     log2(e) folded into one FMA; O is rescaled in TMEM only when the
 //     row max grew by more than 2^8 (exact after the final 1/l);
-//   * the same warpgroup divides by l and stores its rows of out.
+//   * the same warpgroup divides by l and stores its rows of out (f32).
 // TMEM columns (512): S buffers [0,128) and [128,256); with two query tiles
 // P0, P1 at 256, 320 and O0, O1 at 384, 448 (head_dim <= 64); with one query
 // tile P at 256 and O at 320 (head_dim <= 128).
@@ -38,10 +39,9 @@
 
 namespace vattn {
 
-constexpr int kBM = 128;          // query rows per tile (UMMA M)
-constexpr int kBN = 128;          // keys per K/V tile (UMMA N of S, K of P.V)
-constexpr int kThreads = 512;     // 16 warps
-constexpr int kSlotBytes = 32768; // one f32 staging slot
+constexpr int kBM = 128;  // query rows per tile (UMMA M)
+constexpr int kBN = 128;  // keys per K/V tile (UMMA N of S, K of P.V)
+constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 f16
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;                 // lazy-rescale threshold
@@ -49,10 +49,8 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
 
 // g_vattn_status: bit 8 = a wait timed out; low byte = the wait site.
 enum WaitSite : uint32_t {
-  kSiteProducerSlot = 1,
-  kSiteConvSlot = 2,
-  kSiteConvKStage = 3,
-  kSiteConvVStage = 4,
+  kSiteProducerK = 1,
+  kSiteProducerV = 2,
   kSiteMmaQ = 5,
   kSiteMmaK = 6,
   kSiteMmaV = 7,
@@ -69,9 +67,6 @@ constexpr uint32_t kStatusTimeout = 0x100u;
 __device__ uint32_t g_vattn_status;
 
 struct Params {
-  const float* q;
-  const float* k;
-  const float* v;
   float* out;
   int n_patches;  // N
   int head_dim;   // D
@@ -81,49 +76,48 @@ struct Params {
   int vec_out;    // out rows may be written with 16-byte stores
 };
 
-// Shared-memory plan for NQ query tiles and NKB 64-column blocks of head_dim.
+// Shared-memory plan for NQ query tiles and NKB 64-column blocks of d_pad.
 // f16 tiles: NKB blocks of [128 rows x 128 bytes], 128-byte swizzle.
 template <int NQ, int NKB>
 struct Plan {
-  static constexpr int kSlotRows = NKB == 1 ? 128 : 64;  // rows per f32 slot
-  static constexpr int kSubs = 128 / kSlotRows;          // slots per tile
-  static constexpr int kTileF16 = NKB * 128 * 128;
-  static constexpr int kF32Slots = NKB == 1 ? 4 : 2;
+  static constexpr int kThreads = 128 * (1 + NQ);  // control warpgroup + softmax
+  static constexpr int kTileF16 = NKB * kBoxBytes;
+  static constexpr int kStages = NKB == 1 ? 5 : 3;  // K and V stages
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + NQ * kTileF16;
-  static constexpr int kOffV = kOffK + 2 * kTileF16;
-  static constexpr int kOffF32 = kOffV + 2 * kTileF16;
-  static constexpr int kOffBar = kOffF32 + kF32Slots * kSlotBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileF16;
+  static constexpr int kOffBar = kOffV + kStages * kTileF16;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
-  static constexpr int kConvWarps = 16 - 2 - 4 * NQ;
-  static constexpr int kConvThreads = kConvWarps * 32;
-  static constexpr uint32_t kRegsSoftmax = 184;
-  static constexpr uint32_t kRegsOther = NQ == 2 ? 72 : 104;
+  // register split (two query tiles): control warpgroup 56, softmax 224;
+  // launch gives 65536 / 384 -> 168 per thread, 56 + 2 * 224 <= 3 * 168.
+  static constexpr bool kSplitRegs = NQ == 2;
+  static constexpr uint32_t kRegsSoftmax = 224;
+  static constexpr uint32_t kRegsOther = 56;
   // TMEM columns
   static constexpr uint32_t kColP = 256;
   static constexpr uint32_t kColO = NQ == 2 ? 384 : 320;
   static constexpr uint32_t kColStride = 64;  // between the tiles' P (and O) blocks
-  static_assert(NQ * kRegsSoftmax + (4 - NQ) * kRegsOther <= 4 * 128, "register split too large");
+  static_assert(!kSplitRegs || kRegsOther + NQ * kRegsSoftmax <= (1 + NQ) * 168,
+                "register split too large");
   static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
   static_assert(NQ == 1 || NKB == 1, "two query tiles need head_dim <= 64");
 };
 
-// mbarrier indices inside the barrier block.
+// mbarrier indices inside the barrier block (kStages <= 5).
 enum Bar : int {
-  kBarF32Full = 0,    // [4] TMA landed in slot                      (count 1 + tx)
-  kBarF32Empty = 4,   // [4] converters done reading slot            (one per converter warp)
-  kBarKFull = 8,      // [2] f16 K stage written                      (one per converter warp)
-  kBarKEmpty = 10,    // [2] S MMAs done with K stage                (commit)
-  kBarVFull = 12,     // [2] f16 V stage written                      (one per converter warp)
-  kBarVEmpty = 14,    // [2] P.V MMAs done with V stage              (commit)
-  kBarQFull = 16,     // f16 Q tiles written                          (one per converter warp)
-  kBarSFull = 17,     // [2] S buffer complete in TMEM               (commit)
-  kBarSFree = 19,     // [2] S buffer copied to registers            (one per softmax warp)
-  kBarPFull = 21,     // [2] P written, O rescaled (per query tile)  (one per softmax warp)
-  kBarODone = 23,     // [2] P.V complete (per query tile)           (commit)
-  kBarMmaDone = 25,   // every MMA of the block complete             (commit)
-  kNumBars = 26,
+  kBarQFull = 0,      // Q tiles landed                     (1 + tx)
+  kBarKFull = 1,      // [5] K stage landed                 (1 + tx)
+  kBarKEmpty = 6,     // [5] S MMAs done with K stage       (commit)
+  kBarVFull = 11,     // [5] V stage landed                 (1 + tx)
+  kBarVEmpty = 16,    // [5] P.V MMAs done with V stage     (commit)
+  kBarSFull = 21,     // [2] S buffer complete in TMEM      (commit)
+  kBarSFree = 23,     // [2] S buffer(s) copied to registers (one per softmax warp;
+                      //     two query tiles share barrier 0)
+  kBarPFull = 25,     // P of every query tile written, O rescaled (one per softmax warp)
+  kBarODone = 27,     // [2] P.V of query tile complete     (commit)
+  kBarMmaDone = 29,   // every MMA of the block complete    (commit)
+  kNumBars = 30,
 };
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
 constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
@@ -177,97 +171,16 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
 }
 
-// f16 tile address of element chunk (row R, 8-column chunk c): block c/8 of
-// 128 rows x 128 bytes; 16-byte chunk (c%8) ^ (R%8) within the row.
-__device__ __forceinline__ uint32_t f16_chunk_offset(int R, int c) {
-  return static_cast<uint32_t>((c >> 3) * (128 * 128) + R * 128 + (((c & 7) ^ (R & 7)) << 4));
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-  uint4 h;
-  h.x = ptx::pack_half2(x[0], x[1]);
-  h.y = ptx::pack_half2(x[2], x[3]);
-  h.z = ptx::pack_half2(x[4], x[5]);
-  h.w = ptx::pack_half2(x[6], x[7]);
-  return h;
-}
-
-// f32 slot (rows x d_pad, dense) -> f16 tile rows [row_base, row_base+rows).
-// The first (CT / cpr) * cpr converter threads take part (cpr = 8-column
-// chunks per row): thread ct keeps chunk column ct % cpr and walks rows
-// ct / cpr, + CT / cpr, ...  Loads are issued kBatch chunks ahead of their
-// conversion so the shared-memory latencies overlap.
-template <int CT>
-__device__ __forceinline__ void convert_slot(const float* __restrict__ src,
-                                             uint8_t* __restrict__ dst, int row_base, int rows,
-                                             int d_pad, int ct) {
-  constexpr int kBatch = 3;
-  const int cpr = d_pad >> 3;
-  const int dr = CT / cpr;
-  if (ct >= dr * cpr) return;
-  const int c = ct % cpr;
-  // threads with (c & 4) read their upper half first: the 8 threads of a
-  // shared-memory phase then touch all 32 banks once
-  const int sw = c & 4;
-  const float* s0 = src + c * 8;
-  uint8_t* const d0 = dst + (c >> 3) * (128 * 128);
-  const int cc = c & 7;
-  for (int r0 = ct / cpr; r0 < rows; r0 += kBatch * dr) {
-    float4 lo[kBatch], hi[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int r = r0 + u * dr;
-      if (r < rows) {
-        const float* s = s0 + r * d_pad;
-        const float4 x0 = *reinterpret_cast<const float4*>(s + sw);
-        const float4 x1 = *reinterpret_cast<const float4*>(s + (4 - sw));
-        lo[u] = sw ? x1 : x0;
-        hi[u] = sw ? x0 : x1;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int R = row_base + r0 + u * dr;
-      if (r0 + u * dr < rows) {
-        const float x[8] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w, hi[u].x, hi[u].y, hi[u].z, hi[u].w};
-        *reinterpret_cast<uint4*>(d0 + R * 128 + ((cc ^ (R & 7)) << 4)) = pack8(x);
-      }
-    }
-  }
-}
-
-// Global f32 rows (any head_dim, 4-byte aligned) -> f16 tile, zero padding.
-template <int CT>
-__device__ __forceinline__ void convert_global(const float* g, int grow0, int n_rows_valid,
-                                               int D, uint8_t* dst, int d_pad, int ct) {
-  const int cpr = d_pad >> 3;
-  const int dr = CT / cpr, dc = CT % cpr;
-  int r = ct / cpr, c = ct % cpr;
-  while (r < 128) {
-    float x[8];
-    const bool row_ok = r < n_rows_valid;
-    const float* s = g + static_cast<size_t>(grow0 + r) * D;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int d = c * 8 + e;
-      x[e] = (row_ok && d < D) ? __ldg(s + d) : 0.0f;
-    }
-    *reinterpret_cast<uint4*>(dst + f16_chunk_offset(r, c)) = pack8(x);
-    r += dr;
-    c += dc;
-    if (c >= cpr) {
-      c -= cpr;
-      ++r;
-    }
-  }
-}
-
-template <int NQ, int NKB, bool kTma>
-__global__ void __launch_bounds__(kThreads, 1)
+// Grid: B*H * n_qblocks blocks; block = bh * n_qblocks + query block.
+// tm_q / tm_k / tm_v: f16 [B*H, N, d_pad] with boxes of {64 columns, 128 rows},
+// 128-byte swizzle (columns past d_pad and rows past N read as zero).
+template <int NQ, int NKB>
+__global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
     vattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using P = Plan<NQ, NKB>;
+  constexpr int S = P::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = ptx::smem_addr(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -290,23 +203,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sphase = [](int j) -> uint32_t {
     return NQ == 2 ? (static_cast<uint32_t>(j) & 1u) : (static_cast<uint32_t>(j >> 1) & 1u);
   };
+  // barrier telling that the S buffer of key tile j was copied to registers
+  auto sfree_bar = [](int j) -> int { return NQ == 2 ? 0 : (j & 1); };
+  // K/V stage of key tile j and the phase of its barriers
+  auto kv_phase = [](int j) -> uint32_t { return static_cast<uint32_t>(j / S) & 1u; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < P::kF32Slots; ++i) {
-      ptx::mbar_init(bar(kBarF32Full + i), 1);
-      ptx::mbar_init(bar(kBarF32Empty + i), P::kConvWarps);
+    ptx::mbar_init(bar(kBarQFull), 1);
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(bar(kBarKFull + i), 1);
+      ptx::mbar_init(bar(kBarKEmpty + i), 1);
+      ptx::mbar_init(bar(kBarVFull + i), 1);
+      ptx::mbar_init(bar(kBarVEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(bar(kBarKFull + i), P::kConvWarps);
-      ptx::mbar_init(bar(kBarKEmpty + i), 1);
-      ptx::mbar_init(bar(kBarVFull + i), P::kConvWarps);
-      ptx::mbar_init(bar(kBarVEmpty + i), 1);
       ptx::mbar_init(bar(kBarSFull + i), 1);
-      ptx::mbar_init(bar(kBarSFree + i), 4);
-      ptx::mbar_init(bar(kBarPFull + i), 4);
+      ptx::mbar_init(bar(kBarSFree + i), NQ == 2 ? 8 : 4);
+      ptx::mbar_init(bar(kBarPFull + i), 4 * NQ);
       ptx::mbar_init(bar(kBarODone + i), 1);
     }
-    ptx::mbar_init(bar(kBarQFull), P::kConvWarps);
     ptx::mbar_init(bar(kBarMmaDone), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -320,48 +235,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + P::kOffBar + kTmemSlotOff);
 
-  // register split: the softmax warpgroups hold a whole 128-column S row in
-  // registers; the other warpgroups need few.  Sum over the four warpgroups
-  // stays within the 4 x 128 registers per thread the block launched with.
-  const bool softmax_wg = warp >= 4 && warp < 4 + 4 * NQ;
+  const bool softmax_wg = warp >= 4;
   if (!softmax_wg) {
-    ptx::regs_decrease<P::kRegsOther>();
+    if (P::kSplitRegs) ptx::regs_decrease<P::kRegsOther>();
     if (warp == 0) {
       // ---------------------------------------------------------- producer
-      if (kTma && lane == 0) {
+      if (lane == 0) {
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
-        const uint32_t slot_bytes = static_cast<uint32_t>(P::kSlotRows * p.d_pad * 4);
-        int load = 0;
-        bool ok = true;
-        auto issue = [&](const CUtensorMap* tm, int row) {
-          const int slot = load % P::kF32Slots;
-          const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
-          if (!w.wait(bar(kBarF32Empty + slot), (use & 1u) ^ 1u, kSiteProducerSlot)) {
-            ok = false;
-            return;
+        const uint32_t tile_bytes = static_cast<uint32_t>(P::kTileF16);
+        ptx::mbar_arrive_expect_tx(bar(kBarQFull), NQ * tile_bytes);
+        for (int t = 0; t < NQ; ++t)
+          for (int kb = 0; kb < NKB; ++kb)
+            ptx::tma_load_3d(base_s + P::kOffQ + t * P::kTileF16 + kb * kBoxBytes, &tm_q,
+                             bar(kBarQFull), kb * 64, q_row0 + t * kBM, bh);
+        int issued = 0;  // key tiles whose K and V loads were issued
+        for (int j = 0; j < T; ++j) {
+          const int st = j % S;
+          const uint32_t free_par = kv_phase(j) ^ 1u;
+          if (!w.wait(bar(kBarKEmpty + st), free_par, kSiteProducerK)) break;
+          ptx::mbar_arrive_expect_tx(bar(kBarKFull + st), tile_bytes);
+          for (int kb = 0; kb < NKB; ++kb)
+            ptx::tma_load_3d(base_s + P::kOffK + st * P::kTileF16 + kb * kBoxBytes, &tm_k,
+                             bar(kBarKFull + st), kb * 64, j * kBN, bh);
+          if (!w.wait(bar(kBarVEmpty + st), free_par, kSiteProducerV)) {
+            // keep the barrier accounting of the issued K load for the drain
+            issued = -(j + 1);
+            break;
           }
-          ptx::mbar_arrive_expect_tx(bar(kBarF32Full + slot), slot_bytes);
-          ptx::tma_load_3d(base_s + P::kOffF32 + slot * kSlotBytes, tm, bar(kBarF32Full + slot),
-                           0, row, bh);
-          ++load;
-        };
-        for (int t = 0; ok && t < NQ; ++t)
-          for (int s = 0; ok && s < P::kSubs; ++s)
-            issue(&tm_q, q_row0 + t * kBM + s * P::kSlotRows);
-        for (int j = 0; ok && j < T; ++j) {
-          for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_k, j * kBN + s * P::kSlotRows);
-          for (int s = 0; ok && s < P::kSubs; ++s) issue(&tm_v, j * kBN + s * P::kSlotRows);
+          ptx::mbar_arrive_expect_tx(bar(kBarVFull + st), tile_bytes);
+          for (int kb = 0; kb < NKB; ++kb)
+            ptx::tma_load_3d(base_s + P::kOffV + st * P::kTileF16 + kb * kBoxBytes, &tm_v,
+                             bar(kBarVFull + st), kb * 64, j * kBN, bh);
+          issued = j + 1;
         }
-        // the newest copy into each slot must have landed before exit
-        for (int slot = 0; slot < P::kF32Slots; ++slot) {
-          if (load > slot) {
-            const int uses = (load - 1 - slot) / P::kF32Slots + 1;
-            w.drain(bar(kBarF32Full + slot), static_cast<uint32_t>(uses - 1) & 1u,
-                    kSiteDrainTma);
-          }
-        }
+        // every issued copy must have landed before the block exits
+        w.drain(bar(kBarQFull), 0, kSiteDrainTma);
+        const int k_loads = issued >= 0 ? issued : -issued;  // K loads issued
+        const int v_loads = issued >= 0 ? issued : -issued - 1;
+        for (int j = (k_loads > S ? k_loads - S : 0); j < k_loads; ++j)
+          w.drain(bar(kBarKFull + j % S), kv_phase(j), kSiteDrainTma);
+        for (int j = (v_loads > S ? v_loads - S : 0); j < v_loads; ++j)
+          w.drain(bar(kBarVFull + j % S), kv_phase(j), kSiteDrainTma);
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
@@ -372,10 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S(t, j) = Q_t K_j^T into S buffer sbuf(t, j)
         auto issue_s = [&](int t, int j) {
           const uint32_t qa = base_s + P::kOffQ + t * P::kTileF16;
-          const uint32_t kb = base_s + P::kOffK + (j & 1) * P::kTileF16;
+          const uint32_t kb = base_s + P::kOffK + (j % S) * P::kTileF16;
           const uint32_t d = tmem + static_cast<uint32_t>(sbuf(t, j)) * 128u;
           for (int ks = 0; ks < ksteps; ++ks) {
-            const uint32_t off = static_cast<uint32_t>((ks >> 2) * (128 * 128) + (ks & 3) * 32);
+            const uint32_t off = static_cast<uint32_t>((ks >> 2) * kBoxBytes + (ks & 3) * 32);
             ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
                         ptx::smem_desc(kb + off, 16, 1024, ptx::kSwizzle128B), idesc_s,
                         ks > 0 ? 1u : 0u);
@@ -384,12 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // O_t += P_t V_j
         auto issue_pv = [&](int t, int j) {
-          const uint32_t vb = base_s + P::kOffV + (j & 1) * P::kTileF16;
+          const uint32_t vb = base_s + P::kOffV + (j % S) * P::kTileF16;
           const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
           const uint32_t a = tmem + P::kColP + static_cast<uint32_t>(t) * P::kColStride;
           for (int ks = 0; ks < kBN / 16; ++ks) {
             ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
-                        ptx::smem_desc(vb + ks * 2048, 128 * 128, 1024, ptx::kSwizzle128B),
+                        ptx::smem_desc(vb + ks * 2048, kBoxBytes, 1024, ptx::kSwizzle128B),
                         idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
           }
           ptx::mma_commit(bar(kBarODone + t));
@@ -402,86 +318,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit(bar(kBarKEmpty));
         }
         for (int j = 0; ok && j < T; ++j) {
-          const int st = j & 1;
           if (j + 1 < T) {
             // next S as early as possible: it only needs K_{j+1} and the
             // softmax to have copied the previous contents of its buffer
-            const int nst = st ^ 1;
-            if (!(ok = w.wait(bar(kBarKFull + nst), static_cast<uint32_t>((j + 1) >> 1) & 1u,
-                              kSiteMmaK)))
+            const int nst = (j + 1) % S;
+            if (!(ok = w.wait(bar(kBarKFull + nst), kv_phase(j + 1), kSiteMmaK))) break;
+            // one wait per group: the MMAs of both query tiles then issue
+            // back to back (every wait between MMAs leaves the tensor pipe idle)
+            const int prev = NQ == 2 ? j : j - 1;  // last key tile that used the buffer(s)
+            if (prev >= 0 &&
+                !(ok = w.wait(bar(kBarSFree + sfree_bar(prev)), sphase(prev), kSiteMmaSFree)))
               break;
-            for (int t = 0; ok && t < NQ; ++t) {
-              const int prev = NQ == 2 ? j : j - 1;  // last key tile that used this buffer
-              if (prev >= 0 && !(ok = w.wait(bar(kBarSFree + sbuf(t, j + 1)), sphase(prev),
-                                             kSiteMmaSFree)))
-                break;
-              ptx::tc_fence_after();
-              issue_s(t, j + 1);
-            }
-            if (!ok) break;
+            ptx::tc_fence_after();
+            for (int t = 0; t < NQ; ++t) issue_s(t, j + 1);
             ptx::mma_commit(bar(kBarKEmpty + nst));
           }
-          if (!(ok = w.wait(bar(kBarVFull + st), static_cast<uint32_t>(j >> 1) & 1u, kSiteMmaV)))
-            break;
-          for (int t = 0; ok && t < NQ; ++t) {
-            if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
-            ptx::tc_fence_after();
-            issue_pv(t, j);
-          }
-          if (!ok) break;
-          ptx::mma_commit(bar(kBarVEmpty + st));
+          if (!(ok = w.wait(bar(kBarVFull + j % S), kv_phase(j), kSiteMmaV))) break;
+          if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
+          ptx::tc_fence_after();
+          for (int t = 0; t < NQ; ++t) issue_pv(t, j);
+          ptx::mma_commit(bar(kBarVEmpty + j % S));
         }
         ptx::mma_commit(bar(kBarMmaDone));
       }
-    } else {
-      // ---------------------------------------------------------- converters
-      // (warp-uniform waits: every converter lane reaches each warp_arrive)
-      const int ct = (warp < 4 ? warp - 2 : warp - 2 - 4 * NQ) * 32 + lane;
-      constexpr int CT = P::kConvThreads;
-      const size_t head_off = static_cast<size_t>(bh) * N * p.head_dim;
-      int load = 0;
-      bool ok = true;
-      // one 128-row tile (f32 source rows tile_row0..) into the f16 tile at dst
-      auto tile = [&](const float* g, int tile_row0, uint8_t* dst) {
-        if (kTma) {
-          for (int s = 0; s < P::kSubs; ++s) {
-            const int slot = load % P::kF32Slots;
-            const uint32_t use = static_cast<uint32_t>(load / P::kF32Slots);
-            if (!(ok = w.wait_warp(bar(kBarF32Full + slot), use & 1u, kSiteConvSlot))) return;
-            convert_slot<CT>(
-                reinterpret_cast<const float*>(base + P::kOffF32 + slot * kSlotBytes), dst,
-                s * P::kSlotRows, P::kSlotRows, p.d_pad, ct);
-            warp_arrive(bar(kBarF32Empty + slot));
-            ++load;
-          }
-        } else {
-          convert_global<CT>(g + head_off, tile_row0, N - tile_row0, p.head_dim, dst, p.d_pad,
-                             ct);
-        }
-      };
-      for (int t = 0; ok && t < NQ; ++t)
-        tile(p.q, q_row0 + t * kBM, base + P::kOffQ + t * P::kTileF16);
-      if (ok) {
-        ptx::fence_proxy_async_smem();
-        warp_arrive(bar(kBarQFull));
-      }
-      for (int j = 0; ok && j < T; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u;
-        if (!(ok = w.wait_warp(bar(kBarKEmpty + st), ph, kSiteConvKStage))) break;
-        tile(p.k, j * kBN, base + P::kOffK + st * P::kTileF16);
-        if (!ok) break;
-        ptx::fence_proxy_async_smem();
-        warp_arrive(bar(kBarKFull + st));
-        if (!(ok = w.wait_warp(bar(kBarVEmpty + st), ph, kSiteConvVStage))) break;
-        tile(p.v, j * kBN, base + P::kOffV + st * P::kTileF16);
-        if (!ok) break;
-        ptx::fence_proxy_async_smem();
-        warp_arrive(bar(kBarVFull + st));
-      }
     }
   } else {
-    ptx::regs_increase<P::kRegsSoftmax>();
+    if (P::kSplitRegs) ptx::regs_increase<P::kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -506,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld_dep(r[c]);
       ptx::tc_fence_before();
-      warp_arrive(bar(kBarSFree + buf));
+      warp_arrive(bar(kBarSFree + sfree_bar(j)));
 
       if (valid < kBN) {  // ragged last key tile only: keys >= n_patches score -inf
 #pragma unroll
@@ -573,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      warp_arrive(bar(kBarPFull + t));
+      warp_arrive(bar(kBarPFull));
     }
     if (ok && w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(T - 1) & 1u, kSiteEpilogue)) {
       ptx::tc_fence_after();

@@ -1,0 +1,66 @@
+// stage_kernel.cuh -- the f16 staging of q, k and v, once per call.
+//
+// The shader "vision_attention_flash_sub_hpd_f16.wgsl" (rullama 0.1.0)
+// rounds q, k and v to f16 as it copies them into workgroup storage.  Its
+// workgroups re-read and re-round every key/value row once per block of 8
+// queries; here each element is rounded once, into an f16 copy that the
+// attention kernel then streams with TMA straight into the tensor-core
+// operand layout.
+//
+// src: f32 [n_rows, D] (rows of all heads back to back), any alignment of 4;
+// dst: f16 [n_rows, d_pad], d_pad = D rounded up to 16, columns >= D zero,
+//      16-byte aligned rows (d_pad * 2 is a multiple of 32).
+// Rounding: round-to-nearest-even (cvt.rn.f16x2.f32).
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace vattn {
+
+struct StageJob {
+  const float* src;
+  __half* dst;
+};
+
+// Three tensors (q, k, v) of n_rows x D each.  Thread i handles 8-column
+// chunks i, i + stride, ... of the concatenated [3 * n_rows, d_pad / 8]
+// chunk grid.  vec: D % 8 == 0 and 16-byte aligned sources -> two 16-byte
+// loads per chunk; otherwise element loads.
+__global__ void __launch_bounds__(256) vattn_stage_kernel(StageJob a, StageJob b, StageJob c,
+                                                         long long n_rows, int D, int d_pad,
+                                                         int vec) {
+  const int cpr = d_pad >> 3;
+  const long long chunks_per_tensor = n_rows * cpr;
+  const long long total = 3 * chunks_per_tensor;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int which = static_cast<int>(i / chunks_per_tensor);
+    const long long r = i - which * chunks_per_tensor;
+    const long long row = r / cpr;
+    const int ch = static_cast<int>(r - row * cpr);
+    const StageJob job = which == 0 ? a : (which == 1 ? b : c);
+    const float* s = job.src + row * D + ch * 8;
+    float x[8];
+    if (vec && ch * 8 + 8 <= D) {
+      const float4 lo = __ldg(reinterpret_cast<const float4*>(s));
+      const float4 hi = __ldg(reinterpret_cast<const float4*>(s) + 1);
+      x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+      x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = (ch * 8 + e < D) ? __ldg(s + e) : 0.0f;
+    }
+    uint4 h;
+    h.x = ptx::pack_half2(x[0], x[1]);
+    h.y = ptx::pack_half2(x[2], x[3]);
+    h.z = ptx::pack_half2(x[4], x[5]);
+    h.w = ptx::pack_half2(x[6], x[7]);
+    *reinterpret_cast<uint4*>(job.dst + row * d_pad + ch * 8) = h;
+  }
+}
+
+}  // namespace vattn

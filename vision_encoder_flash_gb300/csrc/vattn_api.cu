@@ -1,5 +1,6 @@
 // vattn_api.cu -- the C ABI declared in include/vattn.h: argument checks,
-// tensor-map encoding, variant choice and launch of the sm_103a kernel.
+// workspace, tensor-map encoding, variant choice and the two launches of a
+// call (f16 staging of q/k/v, then the attention kernel) on sm_103a.
 //
 // The operation is the one of the WGSL shader
 // "vision_attention_flash_sub_hpd_f16.wgsl" (rullama 0.1.0): its Params block
@@ -18,6 +19,7 @@
 
 #include "../../include/vattn.h"
 #include "attn_kernel.cuh"
+#include "stage_kernel.cuh"
 
 namespace {
 
@@ -58,24 +60,24 @@ EncodeTiledFn encode_fn() {
   return g_encode;
 }
 
-// 3-D view {head_dim, n_patches, batch*n_heads} of a head-major f32 tensor;
-// one box = slot_rows rows x d_pad columns; out-of-range elements read 0.
-vattn_status make_tmap(CUtensorMap* tm, const float* ptr, int64_t bh, int64_t n, int64_t d,
-                       int d_pad, int slot_rows) {
+// 3-D view {d_pad, n_patches, batch*n_heads} of a head-major f16 tensor; one
+// box = 128 rows x 64 columns (128 bytes), 128-byte swizzle: the layout the
+// tensor-core descriptors expect.  Out-of-range rows and columns read 0.
+vattn_status make_tmap16(CUtensorMap* tm, const __half* ptr, int64_t bh, int64_t n, int d_pad) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     if (g_encode_err != cudaSuccess) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
     return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
   }
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_pad), static_cast<cuuint64_t>(n),
                               static_cast<cuuint64_t>(bh)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4u,
-                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(d) * 4u};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d_pad), static_cast<cuuint32_t>(slot_rows), 1u};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_pad) * 2u,
+                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(d_pad) * 2u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(vattn::kBN), 1u};
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
-  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims,
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(ptr), dims,
                          strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult %d", static_cast<int>(r));
@@ -84,22 +86,50 @@ vattn_status make_tmap(CUtensorMap* tm, const float* ptr, int64_t bh, int64_t n,
 
 constexpr int kMaxDevices = 64;
 
-template <int NQ, int NKB, bool kTma>
-vattn_status launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                    const vattn::Params& p, unsigned grid, cudaStream_t stream, int device) {
-  using P = vattn::Plan<NQ, NKB>;
-  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kTma>;
-  static std::atomic<uint8_t> configured[kMaxDevices];
+// Per-device memory pool for the f16 staging workspace: stream-ordered
+// allocations, memory kept in the pool between calls.
+struct DevicePool {
+  std::once_flag once;
+  cudaMemPool_t pool = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+DevicePool g_pools[kMaxDevices];
+
+vattn_status pool_for(int device, cudaMemPool_t* out) {
   if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
+  DevicePool& dp = g_pools[device];
+  std::call_once(dp.once, [&dp, device] {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = device;
+    dp.err = cudaMemPoolCreate(&dp.pool, &props);
+    if (dp.err == cudaSuccess) {
+      uint64_t keep = UINT64_MAX;
+      dp.err = cudaMemPoolSetAttribute(dp.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+  });
+  if (dp.err != cudaSuccess) return cuda_fail(dp.err, "creating the workspace memory pool");
+  *out = dp.pool;
+  return VATTN_OK;
+}
+
+template <int NQ, int NKB>
+vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const vattn::Params& p, unsigned grid, cudaStream_t stream,
+                              int device) {
+  using P = vattn::Plan<NQ, NKB>;
+  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB>;
+  static std::atomic<uint8_t> configured[kMaxDevices];
   if (!configured[device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          P::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     configured[device].store(1, std::memory_order_release);
   }
-  kernel<<<grid, vattn::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, p);
+  kernel<<<grid, P::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   return VATTN_OK;
 }
 
@@ -147,15 +177,8 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
   const int64_t grid = bh * n_qblocks;
   if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
-  // TMA needs 16-byte aligned bases and row strides (head_dim % 4 == 0)
-  const bool tma = (D % 4 == 0) &&
-                   ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                     reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
 
   vattn::Params p{};
-  p.q = q;
-  p.k = k;
-  p.v = v;
   p.out = out;
   p.n_patches = N;
   p.head_dim = D;
@@ -168,28 +191,51 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  // f16 copies of q, k, v ([B*H, N, d_pad] each), stream-ordered workspace
+  const int64_t rows = bh * N;
+  const size_t region = (static_cast<size_t>(rows) * d_pad * 2 + 255) & ~static_cast<size_t>(255);
+  cudaMemPool_t pool = nullptr;
+  vattn_status st = pool_for(device, &pool);
+  if (st != VATTN_OK) return st;
+  void* ws = nullptr;
+  e = cudaMallocFromPoolAsync(&ws, 3 * region, pool, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  __half* q16 = static_cast<__half*>(ws);
+  __half* k16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + region);
+  __half* v16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + 2 * region);
 
   CUtensorMap tq, tk, tv;
-  std::memset(&tq, 0, sizeof(tq));
-  std::memset(&tk, 0, sizeof(tk));
-  std::memset(&tv, 0, sizeof(tv));
-  const int slot_rows = nkb == 1 ? vattn::Plan<1, 1>::kSlotRows : vattn::Plan<1, 2>::kSlotRows;
-  if (tma) {
-    vattn_status st;
-    if ((st = make_tmap(&tq, q, bh, N, D, d_pad, slot_rows)) != VATTN_OK) return st;
-    if ((st = make_tmap(&tk, k, bh, N, D, d_pad, slot_rows)) != VATTN_OK) return st;
-    if ((st = make_tmap(&tv, v, bh, N, D, d_pad, slot_rows)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tq, q16, bh, N, d_pad)) == VATTN_OK &&
+      (st = make_tmap16(&tk, k16, bh, N, d_pad)) == VATTN_OK &&
+      (st = make_tmap16(&tv, v16, bh, N, d_pad)) == VATTN_OK) {
+    const int vec = (D % 8 == 0) &&
+                    ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                      reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+    const long long chunks = 3LL * rows * (d_pad / 8);
+    const long long blocks = (chunks + 255) / 256;
+    const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
+    vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
+        vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, rows, D, d_pad,
+        vec);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "staging kernel launch");
+    } else {
+      const unsigned g = static_cast<unsigned>(grid);
+      if (nkb == 1 && nq == 2)
+        st = launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
+      else if (nkb == 1)
+        st = launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
+      else
+        st = launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+    }
   }
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const unsigned g = static_cast<unsigned>(grid);
-  if (nkb == 1 && nq == 2)
-    return tma ? launch<2, 1, true>(tq, tk, tv, p, g, stream, device)
-               : launch<2, 1, false>(tq, tk, tv, p, g, stream, device);
-  if (nkb == 1)
-    return tma ? launch<1, 1, true>(tq, tk, tv, p, g, stream, device)
-               : launch<1, 1, false>(tq, tk, tv, p, g, stream, device);
-  return tma ? launch<1, 2, true>(tq, tk, tv, p, g, stream, device)
-             : launch<1, 2, false>(tq, tk, tv, p, g, stream, device);
+  // back to the pool once the launches above have run (stream order)
+  e = cudaFreeAsync(ws, stream);
+  if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
+  return st;
 }
 
 vattn_status vattn_device_status(uint32_t* code) {
