@@ -73,6 +73,47 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
                            int64_t head_dim, void* stream);
 
 /*
+ * Size of the fixed staging scratch of vattn_forward_noalloc: 32 MiB, enough
+ * for batch*n_heads*n_patches*round_up(head_dim, 16) <= 5,592,320 (for
+ * example 16 heads x 4,100 patches at head_dim 72, or 64 heads x 1,024
+ * patches at head_dim 64).
+ */
+#define VATTN_NOALLOC_MAX_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * vattn_forward_noalloc -- vattn_forward without any device memory
+ * allocation.  The shader this library follows has no counterpart: it is an
+ * interface for callers that may not allocate while they run, such as a
+ * plugin inside an inference runtime that owns all device memory and forbids
+ * allocation in its execute step, or a latency-bound loop that cannot take an
+ * allocation's cost or a late out-of-memory failure.
+ *
+ * Arguments, layout, result and error codes are those of vattn_forward.  The
+ * f16 copies of q, k and v go to a fixed array of
+ * VATTN_NOALLOC_MAX_SCRATCH_BYTES that the library's device code holds on
+ * every device it is loaded on (for the life of the process), instead of a
+ * pool allocation; the call makes no cudaMalloc/cudaFree-type call.
+ *
+ * Limit: a problem whose f16 copies (3 x 256-byte-rounded
+ * batch*n_heads*n_patches*round_up(head_dim, 16)*2 bytes) exceed the array is
+ * rejected on the host with VATTN_ERR_UNSUPPORTED and nothing launched; use
+ * vattn_forward for it.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call outside any stream capture.
+ *
+ * Calls that can overlap in time on one device -- on different streams, or
+ * from several host threads -- share the one array and race: their results
+ * are undefined.  Order them (one stream, or events) or use vattn_forward.
+ * Nothing in the array needs to start at zero; each call writes what it
+ * reads.
+ */
+vattn_status vattn_forward_noalloc(const float* q, const float* k, const float* v, float* out,
+                                   int64_t batch, int64_t n_heads, int64_t n_patches,
+                                   int64_t head_dim, void* stream);
+
+/*
  * vattn_device_status -- reads and clears the kernel-side error word of the
  * current device.  Every wait inside the kernel is bounded; one that runs
  * out sets a non-zero code (which wait, in the low byte) and the thread

@@ -18,8 +18,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = _lib.exported_symbols()
-    assert set(names) == {"vattn_forward", "vattn_device_status", "vattn_status_string",
-                          "vattn_last_error_string", "vattn_version"}
+    assert set(names) == {"vattn_forward", "vattn_forward_noalloc", "vattn_device_status",
+                          "vattn_status_string", "vattn_last_error_string", "vattn_version"}
     for name in names:
         assert hasattr(lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.lib_path()], capture_output=True,
@@ -57,11 +57,31 @@ FAKE = 0x10000  # never dereferenced: every case below fails before any CUDA cal
 def test_host_side_argument_errors(lib, args, status):
     assert _lib.forward_status(*args, 0) == status
     assert lib.vattn_last_error_string().decode() != ""
+    # the allocation-free entry point applies the same checks
+    assert _lib.forward_noalloc_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""
+
+
+# f16 staging of 1 x 1 x n x 16: 3 x round_up(n * 32, 256) bytes against the
+# 32 MiB scratch (VATTN_NOALLOC_MAX_SCRATCH_BYTES)
+NOALLOC_MAX_N16 = 32 * 1024 * 1024 // 3 // 256 * 256 // 32
+
+
+@pytest.mark.parametrize("b,h,n,d", [
+    (1, 1, NOALLOC_MAX_N16 + 1, 16),
+    (8, 16, 2304, 64),
+    (1, 64, 1024, 128),
+])
+def test_noalloc_rejects_problems_past_its_scratch_on_the_host(lib, b, h, n, d):
+    assert _lib.forward_noalloc_status(FAKE, FAKE, FAKE, FAKE + 2 ** 40, b, h, n, d, 0) == 2
+    text = lib.vattn_last_error_string().decode()
+    assert "scratch" in text and "vattn_forward" in text
 
 
 @pytest.mark.parametrize("b,h,n", [(0, 4, 10), (2, 0, 10), (2, 4, 0)])
 def test_empty_problems_are_no_ops_even_with_null_pointers(lib, b, h, n):
     assert _lib.forward_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
+    assert _lib.forward_noalloc_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
 
 
 def test_python_binding_rejects_bad_tensors():

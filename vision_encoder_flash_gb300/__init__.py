@@ -9,10 +9,10 @@ missing or no GPU is present the calls raise.
 """
 from __future__ import annotations
 
-from ._lib import (VattnError, device_status, exported_symbols, forward_raw, lib_path,
-                   load_library, status_string, version)
+from ._lib import (VattnError, device_status, exported_symbols, forward_noalloc_raw, forward_raw,
+                   lib_path, load_library, status_string, version)
 
-__all__ = ["forward", "forward_raw", "device_status", "VattnError", "load_library",
+__all__ = ["forward", "forward_raw", "forward_noalloc_raw", "device_status", "VattnError", "load_library",
            "lib_path", "exported_symbols", "status_string", "version"]
 
 

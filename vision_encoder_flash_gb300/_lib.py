@@ -38,6 +38,8 @@ def load_library():
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.vattn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward.restype = ctypes.c_int
+    lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.vattn_forward_noalloc.restype = ctypes.c_int
     lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.vattn_device_status.restype = ctypes.c_int
     lib.vattn_status_string.argtypes = [ctypes.c_int]
@@ -68,6 +70,22 @@ def forward_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head
     """Like forward_raw but returns the status code instead of raising."""
     return int(load_library().vattn_forward(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                             n_patches, head_dim, stream))
+
+
+def forward_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int,
+                        n_heads: int, n_patches: int, head_dim: int, stream: int = 0) -> None:
+    """Direct call of vattn_forward_noalloc: the allocation-free variant, for
+    callers that may not allocate device memory while they run.  Its staging
+    scratch is one fixed array per device, so calls that overlap in time race."""
+    _check(load_library().vattn_forward_noalloc(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                                n_patches, head_dim, stream))
+
+
+def forward_noalloc_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,
+                           stream=0) -> int:
+    """Like forward_noalloc_raw but returns the status code instead of raising."""
+    return int(load_library().vattn_forward_noalloc(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                                    n_patches, head_dim, stream))
 
 
 def device_status() -> int:

@@ -276,3 +276,138 @@ const char* vattn_last_error_string(void) { return g_last_error; }
 int vattn_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  Some callers may not allocate device memory while
+// the attention runs: a plugin executed by an inference runtime that owns all
+// device memory and forbids allocation inside its execute step, or a latency-
+// bound loop that cannot take an allocation's cost or a late out-of-memory
+// failure.  vattn_forward_noalloc serves them: its f16 staging copies of q, k
+// and v live in a fixed array in the library image instead of the memory pool
+// that vattn_forward draws from.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(VATTN_NOALLOC_MAX_SCRATCH_BYTES);
+
+// One instance per device, created when the library's device code is loaded
+// on that device and kept until the process exits; every call of
+// vattn_forward_noalloc on the device shares it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+// Device address of g_noalloc_scratch on `device`, which must be current:
+// looked up on the first call per device, then cached.  A failed lookup is
+// not cached, so a later call tries again.
+vattn_status noalloc_scratch(int device, uint8_t** out) {
+  if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
+  void* addr = g_noalloc_addr[device].load(std::memory_order_acquire);
+  if (!addr) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    addr = g_noalloc_addr[device].load(std::memory_order_relaxed);
+    if (!addr) {
+      const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the staging scratch");
+      g_noalloc_addr[device].store(addr, std::memory_order_release);
+    }
+  }
+  *out = static_cast<uint8_t*>(addr);
+  return VATTN_OK;
+}
+
+}  // namespace
+
+extern "C" vattn_status vattn_forward_noalloc(const float* q, const float* k, const float* v,
+                                              float* out, int64_t batch, int64_t n_heads,
+                                              int64_t n_patches, int64_t head_dim,
+                                              void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks (the rules of vattn_forward plus the scratch size),
+  //      before any CUDA call
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
+                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (head_dim > VATTN_MAX_HEAD_DIM)
+    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
+  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
+  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+
+  const int D = static_cast<int>(head_dim);
+  const int N = static_cast<int>(n_patches);
+  const int d_pad = (D + 15) & ~15;
+  const int64_t rows = bh * N;
+  // bh * N < 2^62 / head_dim here, so these products do not overflow
+  const uint64_t region = (static_cast<uint64_t>(rows) * d_pad * 2u + 255u) & ~uint64_t{255};
+  if (region > kNoAllocScratchBytes / 3)
+    return fail(VATTN_ERR_UNSUPPORTED,
+                "problem needs %llu bytes of f16 staging scratch (3 x batch*n_heads*n_patches x "
+                "round_up(head_dim, 16) x 2); vattn_forward_noalloc has %llu "
+                "(VATTN_NOALLOC_MAX_SCRATCH_BYTES): call vattn_forward instead",
+                (unsigned long long)(3u * region), (unsigned long long)kNoAllocScratchBytes);
+  const int nkb = d_pad <= 64 ? 1 : 2;
+  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+
+  vattn::Params p{};
+  p.out = out;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = d_pad;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+
+  // ---- device side
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  uint8_t* ws = nullptr;
+  vattn_status st = noalloc_scratch(device, &ws);
+  if (st != VATTN_OK) return st;
+  __half* q16 = reinterpret_cast<__half*>(ws);
+  __half* k16 = reinterpret_cast<__half*>(ws + region);
+  __half* v16 = reinterpret_cast<__half*>(ws + 2 * region);
+
+  CUtensorMap tq, tk, tv;
+  if ((st = make_tmap16(&tq, q16, bh, N, d_pad)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tk, k16, bh, N, d_pad)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tv, v16, bh, N, d_pad)) != VATTN_OK) return st;
+
+  // Nothing in the scratch has to start at zero: the staging kernel writes
+  // every f16 element the attention kernel reads (padding columns included),
+  // and rows past n_patches are never read from memory (the tensor maps
+  // return zeros there).
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int vec = (D % 8 == 0) &&
+                  ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                    reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+  const long long chunks = 3LL * rows * (d_pad / 8);
+  const long long blocks = (chunks + 255) / 256;
+  const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
+  vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
+      vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, rows, D, d_pad,
+      vec);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
+  const unsigned g = static_cast<unsigned>(grid);
+  if (nkb == 1 && nq == 2) return launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
+  if (nkb == 1) return launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
+  return launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+}
