@@ -14,11 +14,13 @@
 //   * warp 0 streams the f16 Q, K and V tiles with TMA
 //     (cp.async.bulk.tensor, 128-byte swizzle) straight into the layout the
 //     tensor core reads; rows past n_patches read as zero;
-//   * warp 1 issues tcgen05.mma: S = Q K^T (f32 in TMEM), then O += P V with
-//     P taken from TMEM and V from shared memory.  S and P have separate
-//     TMEM columns, so the next S = Q K^T is issued as soon as the softmax
-//     has copied the current S into registers and runs while the softmax
-//     computes its exponentials;
+//   * warp 1 issues the tcgen05.mma of S = Q K^T (f32 in TMEM), warp 2
+//     those of O += P V (P from TMEM, V from shared memory).  Each waits at
+//     one point per key tile, so one keeps the tensor core busy while the
+//     other waits or is held back by the softmax warps on its scheduler.
+//     S and P have separate TMEM columns: the next S = Q K^T is issued as
+//     soon as the softmax has copied the current S into registers, and the
+//     softmax computes its exponentials while the previous P V still runs;
 //   * one warpgroup per query tile runs the online softmax: thread = query
 //     row, so the row max and row sum need no shuffles; exp is exp2 with
 //     log2(e) folded into one FMA; O is rescaled in TMEM only when the
@@ -116,7 +118,7 @@ enum Bar : int {
                       //     two query tiles share barrier 0)
   kBarPFull = 25,     // P of every query tile written, O rescaled (one per softmax warp)
   kBarODone = 27,     // [2] P.V of query tile complete     (commit)
-  kBarMmaDone = 29,   // every MMA of the block complete    (commit)
+  kBarMmaDone = 29,   // every MMA of the block complete    (one commit per issuer)
   kNumBars = 30,
 };
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
       ptx::mbar_init(bar(kBarPFull + i), 4 * NQ);
       ptx::mbar_init(bar(kBarODone + i), 1);
     }
-    ptx::mbar_init(bar(kBarMmaDone), 1);
+    ptx::mbar_init(bar(kBarMmaDone), 2);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -279,13 +281,15 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
         for (int j = (v_loads > S ? v_loads - S : 0); j < v_loads; ++j)
           w.drain(bar(kBarVFull + j % S), kv_phase(j), kSiteDrainTma);
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
-        const uint32_t idesc_s = ptx::idesc_f16_f32(kBM, kBN, false);
-        const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
-        const int ksteps = p.d_pad >> 4;
+    } else if (warp == 1 || warp == 2) {
+      // ---------------------------------------------------------- MMA issuers
+      // Two threads issue tcgen05.mma: the S products depend on the softmax
+      // having copied S out, the P V products on P being written, and on
+      // nothing else of each other, so each issuer waits once per key tile.
+      if (lane == 0 && warp == 1) {
         // S(t, j) = Q_t K_j^T into S buffer sbuf(t, j)
+        const uint32_t idesc_s = ptx::idesc_f16_f32(kBM, kBN, false);
+        const int ksteps = p.d_pad >> 4;
         auto issue_s = [&](int t, int j) {
           const uint32_t qa = base_s + P::kOffQ + t * P::kTileF16;
           const uint32_t kb = base_s + P::kOffK + (j % S) * P::kTileF16;
@@ -298,7 +302,29 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
           }
           ptx::mma_commit(bar(kBarSFull + sbuf(t, j)));
         };
+        bool ok = w.wait(bar(kBarQFull), 0, kSiteMmaQ) && w.wait(bar(kBarKFull), 0, kSiteMmaK);
+        if (ok) {
+          ptx::tc_fence_after();
+          for (int t = 0; t < NQ; ++t) issue_s(t, 0);
+          ptx::mma_commit(bar(kBarKEmpty));
+        }
+        for (int j = 0; ok && j + 1 < T; ++j) {
+          // S of key tile j+1 needs K_{j+1} and the softmax to have copied
+          // the previous contents of its buffer(s) to registers
+          const int nst = (j + 1) % S;
+          if (!(ok = w.wait(bar(kBarKFull + nst), kv_phase(j + 1), kSiteMmaK))) break;
+          const int prev = NQ == 2 ? j : j - 1;  // last key tile that used the buffer(s)
+          if (prev >= 0 &&
+              !(ok = w.wait(bar(kBarSFree + sfree_bar(prev)), sphase(prev), kSiteMmaSFree)))
+            break;
+          ptx::tc_fence_after();
+          for (int t = 0; t < NQ; ++t) issue_s(t, j + 1);
+          ptx::mma_commit(bar(kBarKEmpty + nst));
+        }
+        ptx::mma_commit(bar(kBarMmaDone));
+      } else if (lane == 0 && warp == 2) {
         // O_t += P_t V_j
+        const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
         auto issue_pv = [&](int t, int j) {
           const uint32_t vb = base_s + P::kOffV + (j % S) * P::kTileF16;
           const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
@@ -310,29 +336,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
           }
           ptx::mma_commit(bar(kBarODone + t));
         };
-
-        bool ok = w.wait(bar(kBarQFull), 0, kSiteMmaQ) && w.wait(bar(kBarKFull), 0, kSiteMmaK);
-        if (ok) {
-          ptx::tc_fence_after();
-          for (int t = 0; t < NQ; ++t) issue_s(t, 0);
-          ptx::mma_commit(bar(kBarKEmpty));
-        }
+        bool ok = true;
         for (int j = 0; ok && j < T; ++j) {
-          if (j + 1 < T) {
-            // next S as early as possible: it only needs K_{j+1} and the
-            // softmax to have copied the previous contents of its buffer
-            const int nst = (j + 1) % S;
-            if (!(ok = w.wait(bar(kBarKFull + nst), kv_phase(j + 1), kSiteMmaK))) break;
-            // one wait per group: the MMAs of both query tiles then issue
-            // back to back (every wait between MMAs leaves the tensor pipe idle)
-            const int prev = NQ == 2 ? j : j - 1;  // last key tile that used the buffer(s)
-            if (prev >= 0 &&
-                !(ok = w.wait(bar(kBarSFree + sfree_bar(prev)), sphase(prev), kSiteMmaSFree)))
-              break;
-            ptx::tc_fence_after();
-            for (int t = 0; t < NQ; ++t) issue_s(t, j + 1);
-            ptx::mma_commit(bar(kBarKEmpty + nst));
-          }
           if (!(ok = w.wait(bar(kBarVFull + j % S), kv_phase(j), kSiteMmaV))) break;
           if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
           ptx::tc_fence_after();
@@ -392,8 +397,31 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
       const float alpha = ptx::ex2_approx(m_ref - m_new);  // 0 on the first tile, 1 if kept
       m_ref = m_new;
 
+      // p = 2^(s*log2e - m_ref) as f16 pairs, kept in registers: the P
+      // buffer may still be read by the previous key tile's P V, which runs
+      // on the tensor core meanwhile
+      const float2 scale = make_float2(kLog2e, kLog2e);
+      const float2 shift = make_float2(-m_ref, -m_ref);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
+      uint32_t pk[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), scale,
+              shift);
+          const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
+          pk[c][i] = ptx::pack_half2(pp.x, pp.y);
+        }
+      }
+      const float2 s01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 s23 = __fadd2_rn(acc[2], acc[3]);
+      l = fmaf(l, alpha, (s01.x + s01.y) + (s23.x + s23.y));
       if (j > 0) {
-        // P.V of the previous key tile has finished: P buffer free, O final
+        // P V of the previous key tile has finished: P buffer free, O final
         if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(j - 1) & 1u,
                                kSiteSoftO)))
           break;
@@ -409,29 +437,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
           }
         }
       }
-
-      // p = 2^(s*log2e - m_ref), stored as f16 pairs in this tile's P buffer
-      const float2 scale = make_float2(kLog2e, kLog2e);
-      const float2 shift = make_float2(-m_ref, -m_ref);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x = __ffma2_rn(
-              make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), scale,
-              shift);
-          const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-          acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
-          pk[i] = ptx::pack_half2(pp.x, pp.y);
-        }
-        ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk);
-      }
-      const float2 s01 = __fadd2_rn(acc[0], acc[1]);
-      const float2 s23 = __fadd2_rn(acc[2], acc[3]);
-      l = fmaf(l, alpha, (s01.x + s01.y) + (s23.x + s23.y));
+      for (int c = 0; c < 4; ++c) ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk[c]);
 
       ptx::tmem_wait_st();
       ptx::tc_fence_before();

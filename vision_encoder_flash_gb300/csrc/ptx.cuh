@@ -43,18 +43,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // Probe of a phase: true once the phase of parity `parity` has completed.
-// The thread may be suspended in hardware for up to kSuspendHintNs while
-// the phase is pending, so a waiting warp does not spin on issue slots.
-constexpr uint32_t kSuspendHintNs = 1000000;
-
+// While the phase is pending the thread may be suspended for a short,
+// hardware-chosen time.  (An explicit suspend-time hint made the waits of
+// the attention pipeline measurably slower.)
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
 }
@@ -235,6 +234,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(swizzle & 7u) << 61;
   return d;
+}
+
+// The same descriptor split in two 32-bit halves, so that an issue loop only
+// adds (byte offset >> 4) to the low half: the start-address field (14 bits)
+// does not overflow for shared-memory addresses below 256 KB.
+__device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t smem_desc_hi(uint32_t sbo_bytes, uint32_t swizzle) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | ((swizzle & 7u) << 29);
+}
+__device__ __forceinline__ uint64_t smem_desc_join(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Instruction descriptor for kind::f16 with f16 A/B and f32 accumulator.
