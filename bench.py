@@ -320,10 +320,37 @@ def run_vattn(args, workload):
     clocks = sampler.summary(host_t0, host_t1)
 
     ms_per_step = max_over_ranks(total_ms / args.steps, pg, dev)
-    kernel_ms = max_over_ranks(sum(launch_ms) / len(launch_ms), pg, dev)
+    call_ms = max_over_ranks(sum(launch_ms) / len(launch_ms), pg, dev)
     flops = float(workload.flops)
     value = weak_scaling_value(flops, world, ms_per_step)
+
+    # ---- the dominant kernel alone: vattn_forward_f16 launches exactly the
+    # attention kernel of a step, on the same workload rounded to f16 once
+    # (untimed preparation); per-launch events on the same stream
+    q16, k16, v16 = (x.half() for x in (qd, kd, vd))
+    ptrs16 = (q16.data_ptr(), k16.data_ptr(), v16.data_ptr(), out.data_ptr(), B, H, N, D, sp)
+    for _ in range(args.warmup):
+        vef.forward_f16_raw(*ptrs16)
+    torch.cuda.synchronize(dev)
+    n_attn = max(3, min(args.steps, 1000))
+    ev16 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n_attn)]
+    for s, e in ev16:
+        s.record(stream)
+        vef.forward_f16_raw(*ptrs16)
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    if vef.device_status() != 0:
+        raise RuntimeError("kernel reported a wait timeout")
+    attn_ms = [s.elapsed_time(e) for s, e in ev16]
+    kernel_ms = max_over_ranks(sum(attn_ms) / len(attn_ms), pg, dev)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
+    del q16, k16, v16
+    # the staging kernel: the rest of a call; HBM bytes read (3 f32 tensors)
+    # and written (3 f16 tensors of rows padded to 16 elements)
+    stage_ms = max(call_ms - kernel_ms, 1e-6)
+    d_pad = (D + 15) // 16 * 16
+    stage_bytes = 3 * B * H * N * (4 * D + 2 * d_pad)
 
     pk, pk_src = peaks()
     peak_tf = float(pk["bf16_tflops"]) * F16_OVER_BF16_NOMINAL
@@ -396,15 +423,21 @@ def run_vattn(args, workload):
                      "frac": achieved / peak_tf, "traffic": traffic_from_profile(),
                      "peak_source": f"{pk_src} bf16_tflops (burst) x {F16_OVER_BF16_NOMINAL} "
                                     f"(f16/bf16 nominal ratio)",
-                     "kernel_ms": kernel_ms,
+                     "kernel": "vattn_fwd_kernel (attention; timed alone through vattn_forward_f16)",
+                     "kernel_ms": kernel_ms, "launches_timed": n_attn,
                      "frac_of_sustained": achieved / (float(pk.get("bf16_tflops_sustained", peak_tf))
-                                                      * F16_OVER_BF16_NOMINAL)},
+                                                      * F16_OVER_BF16_NOMINAL),
+                     "stage_kernel": {"bound": "hbm", "ms": stage_ms, "bytes": stage_bytes,
+                                      "achieved_gbs": stage_bytes / (stage_ms * 1e-3) / 1e9,
+                                      "peak_gbs": float(pk["hbm_gbs"]),
+                                      "frac": stage_bytes / (stage_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
+                                      "how": "per-call time minus the attention kernel's time"}},
         "cpu_baseline": cpu_baseline,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "path": "vision_encoder_flash_gb300.forward on pinned host tensors"},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,  # staging kernel + attention kernel per step
         "other_workloads": extras,
     }
     print(json.dumps(line), flush=True)

@@ -73,6 +73,34 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
                            int64_t head_dim, void* stream);
 
 /*
+ * vattn_forward_f16 -- the same attention on inputs that are already f16.
+ *
+ * The shader rounds q, k and v to f16 as it stages them in workgroup
+ * storage (its q_shared / kv_tile declarations); vattn_forward does that
+ * rounding in a first kernel.  Callers whose activations are already f16
+ * skip it here: this call launches the attention kernel alone, which reads
+ * the caller's tensors directly with TMA.  The result equals vattn_forward
+ * on the f32 values of these f16 inputs (the same kernel, the same
+ * arithmetic).
+ *
+ * q, k, v: DEVICE pointers to contiguous IEEE binary16 tensors (bit
+ *   patterns as uint16_t) of shape [batch, n_heads, n_patches, head_dim],
+ *   head-major, q pre-scaled; 16-byte aligned.
+ * out: DEVICE pointer to f32 [batch, n_heads, n_patches, head_dim], 4-byte
+ *   aligned, not overlapping q, k or v.  The caller owns all buffers.
+ * head_dim: 8..128, a multiple of 8 (rows must span whole 16-byte units);
+ *   other values return VATTN_ERR_UNSUPPORTED (use vattn_forward).
+ * stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *
+ * Asynchronous, no allocation, one kernel launch; empty problems are a
+ * no-op.  Errors as for vattn_forward (argument errors on the host before
+ * any CUDA call).
+ */
+vattn_status vattn_forward_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               float* out, int64_t batch, int64_t n_heads, int64_t n_patches,
+                               int64_t head_dim, void* stream);
+
+/*
  * Size of the fixed staging scratch of vattn_forward_noalloc: 32 MiB, enough
  * for batch*n_heads*n_patches*round_up(head_dim, 16) <= 5,592,320 (for
  * example 16 heads x 4,100 patches at head_dim 72, or 64 heads x 1,024

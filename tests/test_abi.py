@@ -18,8 +18,9 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = _lib.exported_symbols()
-    assert set(names) == {"vattn_forward", "vattn_forward_noalloc", "vattn_device_status",
-                          "vattn_status_string", "vattn_last_error_string", "vattn_version"}
+    assert set(names) == {"vattn_forward", "vattn_forward_f16", "vattn_forward_noalloc",
+                          "vattn_device_status", "vattn_status_string",
+                          "vattn_last_error_string", "vattn_version"}
     for name in names:
         assert hasattr(lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.lib_path()], capture_output=True,
@@ -60,6 +61,39 @@ def test_host_side_argument_errors(lib, args, status):
     # the allocation-free entry point applies the same checks
     assert _lib.forward_noalloc_status(*args, 0) == status
     assert lib.vattn_last_error_string().decode() != ""
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, -1, 2, 3, 8), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 0), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 136), 2),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 12), 2),      # head_dim % 8 != 0
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 1), 2),
+    ((0, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8), 1),
+    ((FAKE + 8, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8), 3),  # f16 inputs need 16 bytes
+    ((FAKE, FAKE, FAKE + 2, FAKE + 2 ** 30, 1, 2, 3, 8), 3),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30 + 2, 1, 2, 3, 8), 3),
+    # out (f32, 2x the bytes) overlaps v: v's 96 bytes start 64 bytes after out
+    ((FAKE + 2 ** 20, FAKE + 2 ** 21, FAKE + 64, FAKE, 1, 2, 3, 8), 1),
+    ((FAKE, FAKE, FAKE, FAKE, 1, 1, 2 ** 31, 8), 2),
+])
+def test_f16_entry_host_side_argument_errors(lib, args, status):
+    assert _lib.forward_f16_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""
+
+
+@pytest.mark.parametrize("b,h,n", [(0, 4, 10), (2, 0, 10), (2, 4, 0)])
+def test_f16_entry_empty_problems_are_no_ops(lib, b, h, n):
+    assert _lib.forward_f16_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
+
+
+def test_f16_binding_rejects_bad_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 2, 3, 8, dtype=torch.float16)
+    with pytest.raises(TypeError):
+        vef.forward_f16(q.float(), q, q)
+    with pytest.raises(ValueError):
+        vef.forward_f16(q, q, q)  # CPU tensors
 
 
 # f16 staging of 1 x 1 x n x 16: 3 x round_up(n * 32, 256) bytes against the

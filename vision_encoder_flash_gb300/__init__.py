@@ -9,10 +9,12 @@ missing or no GPU is present the calls raise.
 """
 from __future__ import annotations
 
-from ._lib import (VattnError, device_status, exported_symbols, forward_noalloc_raw, forward_raw,
-                   lib_path, load_library, status_string, version)
+from ._lib import (VattnError, device_status, exported_symbols, forward_f16_raw,
+                   forward_noalloc_raw, forward_raw, lib_path, load_library, status_string,
+                   version)
 
-__all__ = ["forward", "forward_raw", "forward_noalloc_raw", "device_status", "VattnError", "load_library",
+__all__ = ["forward", "forward_f16", "forward_raw", "forward_f16_raw", "forward_noalloc_raw",
+           "device_status", "VattnError", "load_library",
            "lib_path", "exported_symbols", "status_string", "version"]
 
 
@@ -61,6 +63,38 @@ def forward(q, k, v, out=None, stream=None):
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     _launch(q, k, v, out, s)
+    return out
+
+
+def forward_f16(q, k, v, out=None, stream=None):
+    """out (f32) = softmax(q k^T) v for CUDA float16 tensors ``[B, H, N, D]``,
+    ``D`` a multiple of 8; the attention kernel reads the f16 tensors directly
+    (no conversion pass).  Runs on ``stream`` (default: the current torch
+    stream) and returns ``out`` without synchronising."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.float16:
+            raise TypeError(f"{name} must be float16, got {t.dtype}")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [batch, n_heads, n_patches, head_dim]")
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (head-major [B, H, N, D])")
+    if not (q.shape == k.shape == v.shape) or not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must have one shape and one device")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.float32 or out.device != q.device \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor of q's shape and device")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    B, H, N, D = q.shape
+    forward_f16_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D,
+                    s.cuda_stream)
     return out
 
 

@@ -38,6 +38,8 @@ def load_library():
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.vattn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward.restype = ctypes.c_int
+    lib.vattn_forward_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.vattn_forward_f16.restype = ctypes.c_int
     lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_noalloc.restype = ctypes.c_int
     lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -70,6 +72,20 @@ def forward_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head
     """Like forward_raw but returns the status code instead of raising."""
     return int(load_library().vattn_forward(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                             n_patches, head_dim, stream))
+
+
+def forward_f16_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int, n_heads: int,
+                    n_patches: int, head_dim: int, stream: int = 0) -> None:
+    """Direct call of vattn_forward_f16: f16 q, k, v (device addresses), f32 out."""
+    _check(load_library().vattn_forward_f16(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                            n_patches, head_dim, stream))
+
+
+def forward_f16_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,
+                       stream=0) -> int:
+    """Like forward_f16_raw but returns the status code instead of raising."""
+    return int(load_library().vattn_forward_f16(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                                n_patches, head_dim, stream))
 
 
 def forward_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int,
@@ -110,4 +126,4 @@ def exported_symbols() -> list[str]:
     with open(HEADER) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(vattn_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(vattn_[a-z0-9_]+)\s*\(", text)))

@@ -60,19 +60,20 @@ EncodeTiledFn encode_fn() {
   return g_encode;
 }
 
-// 3-D view {d_pad, n_patches, batch*n_heads} of a head-major f16 tensor; one
-// box = 128 rows x 64 columns (128 bytes), 128-byte swizzle: the layout the
-// tensor-core descriptors expect.  Out-of-range rows and columns read 0.
-vattn_status make_tmap16(CUtensorMap* tm, const __half* ptr, int64_t bh, int64_t n, int d_pad) {
+// 3-D view {cols, n_patches, batch*n_heads} of a head-major f16 tensor whose
+// rows hold `cols` elements; one box = 128 rows x 64 columns (128 bytes),
+// 128-byte swizzle: the layout the tensor-core descriptors expect.
+// Out-of-range rows and columns read 0.  cols * 2 must be a multiple of 16.
+vattn_status make_tmap16(CUtensorMap* tm, const __half* ptr, int64_t bh, int64_t n, int cols) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     if (g_encode_err != cudaSuccess) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
     return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
   }
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_pad), static_cast<cuuint64_t>(n),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(n),
                               static_cast<cuuint64_t>(bh)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_pad) * 2u,
-                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(d_pad) * 2u};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2u,
+                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(cols) * 2u};
   const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(vattn::kBN), 1u};
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
   const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(ptr), dims,
@@ -136,6 +137,12 @@ vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, cons
 bool overlaps(const void* a, const void* b, uint64_t bytes) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + bytes && y < x + bytes;
+}
+
+// [a, a + a_bytes) and [b, b + b_bytes) intersect
+bool overlaps2(const void* a, uint64_t a_bytes, const void* b, uint64_t b_bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + b_bytes && y < x + a_bytes;
 }
 
 }  // namespace
@@ -236,6 +243,77 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   e = cudaFreeAsync(ws, stream);
   if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
   return st;
+}
+
+vattn_status vattn_forward_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               float* out, int64_t batch, int64_t n_heads, int64_t n_patches,
+                               int64_t head_dim, void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks, before any CUDA call
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
+                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (head_dim > VATTN_MAX_HEAD_DIM)
+    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  if (head_dim % 8 != 0)
+    return fail(VATTN_ERR_UNSUPPORTED,
+                "f16 inputs need head_dim %% 8 == 0 (16-byte rows), got %lld: use vattn_forward",
+                (long long)head_dim);
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t in_bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 2u;
+  const uint64_t out_bytes = 2u * in_bytes;
+  if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+        reinterpret_cast<uintptr_t>(v)) & 15u) != 0)
+    return fail(VATTN_ERR_MISALIGNED, "f16 q, k, v must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(out) & 3u)
+    return fail(VATTN_ERR_MISALIGNED, "out must be 4-byte aligned");
+  if (overlaps2(out, out_bytes, q, in_bytes) || overlaps2(out, out_bytes, k, in_bytes) ||
+      overlaps2(out, out_bytes, v, in_bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+
+  const int D = static_cast<int>(head_dim);
+  const int N = static_cast<int>(n_patches);
+  const int d_pad = (D + 15) & ~15;
+  const int nkb = d_pad <= 64 ? 1 : 2;
+  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+
+  vattn::Params p{};
+  p.out = out;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = d_pad;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+
+  // ---- device side: the tensor maps read the caller's rows of D elements;
+  // columns D..d_pad-1 read as zero
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
+  CUtensorMap tq, tk, tv;
+  vattn_status st;
+  if ((st = make_tmap16(&tq, reinterpret_cast<const __half*>(q), bh, N, D)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tk, reinterpret_cast<const __half*>(k), bh, N, D)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tv, reinterpret_cast<const __half*>(v), bh, N, D)) != VATTN_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const unsigned g = static_cast<unsigned>(grid);
+  if (nkb == 1 && nq == 2) return launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
+  if (nkb == 1) return launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
+  return launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
 }
 
 vattn_status vattn_device_status(uint32_t* code) {
