@@ -10,8 +10,11 @@
 // [B*H, N, d_pad] f16, d_pad = head_dim rounded up to 16, zero padding.
 // The shader's design (8 queries x 32 keys per 64-thread workgroup, scalar
 // dot products, subgroup reductions) is replaced by a GB300 one:
-//   * one thread block = one bh and NQ query tiles of 128 rows;
-//   * warp 0 streams the f16 Q, K and V tiles with TMA
+//   * a work tile = one bh and NQ query tiles of 128 rows; the grid is one
+//     block per multiprocessor and each block loops over its tiles, so
+//     barrier setup and TMEM allocation happen once, and the next tile's
+//     K/V and Q loads and first S = Q K^T overlap the end of the current one;
+//   * warp 0 streams the f16 K and V tiles, warp 3 the Q tiles, with TMA
 //     (cp.async.bulk.tensor, 128-byte swizzle) straight into the layout the
 //     tensor core reads; rows past n_patches read as zero;
 //   * warp 1 issues the tcgen05.mma of S = Q K^T (f32 in TMEM), warp 2
@@ -53,6 +56,7 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
 enum WaitSite : uint32_t {
   kSiteProducerK = 1,
   kSiteProducerV = 2,
+  kSiteProducerQ = 3,
   kSiteMmaQ = 5,
   kSiteMmaK = 6,
   kSiteMmaV = 7,
@@ -73,9 +77,11 @@ struct Params {
   int n_patches;  // N
   int head_dim;   // D
   int d_pad;      // D rounded up to 16
-  int n_qblocks;  // thread blocks per bh
+  int n_qblocks;  // query blocks (NQ tiles of 128 rows) per bh
+  int n_tiles;    // bh * n_qblocks units of work, spread over the grid
   int n_ktiles;   // ceil(N / kBN)
   int vec_out;    // out rows may be written with 16-byte stores
+  int tma_out;    // write out through tm_o (TMA stores; head_dim <= 64, % 4 == 0)
 };
 
 // Shared-memory plan for NQ query tiles and NKB 64-column blocks of d_pad.
@@ -88,7 +94,11 @@ struct Plan {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + NQ * kTileF16;
   static constexpr int kOffV = kOffK + kStages * kTileF16;
-  static constexpr int kOffBar = kOffV + kStages * kTileF16;
+  // output staging for the TMA-store epilogue (head_dim <= 64 only): two
+  // 2 KB buffers (32 rows x 16 f32, 64-byte swizzle) per softmax warp
+  static constexpr int kEpiBytes = NKB == 1 ? 4 * NQ * 4096 : 0;
+  static constexpr int kOffEpi = kOffV + kStages * kTileF16;
+  static constexpr int kOffBar = kOffEpi + kEpiBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   // register split (two query tiles): control warpgroup 56, softmax 224;
@@ -119,7 +129,8 @@ enum Bar : int {
   kBarPFull = 25,     // P of every query tile written, O rescaled (one per softmax warp)
   kBarODone = 27,     // [2] P.V of query tile complete     (commit)
   kBarMmaDone = 29,   // every MMA of the block complete    (one commit per issuer)
-  kNumBars = 30,
+  kBarQEmpty = 30,    // S products of a tile done with its Q tiles (commit)
+  kNumBars = 31,
 };
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
 constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
@@ -173,14 +184,16 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
 }
 
-// Grid: B*H * n_qblocks blocks; block = bh * n_qblocks + query block.
+// Persistent: tile = bh * n_qblocks + query block, n_tiles in all; block b
+// handles tiles b, b + gridDim.x, ... (gridDim.x <= n_tiles).
 // tm_q / tm_k / tm_v: f16 [B*H, N, d_pad] with boxes of {64 columns, 128 rows},
 // 128-byte swizzle (columns past d_pad and rows past N read as zero).
 template <int NQ, int NKB>
 __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
     vattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o, const Params p) {
   using P = Plan<NQ, NKB>;
   constexpr int S = P::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -195,23 +208,32 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / p.n_qblocks;
-  const int q_row0 = (blockIdx.x % p.n_qblocks) * (kBM * NQ);
   const int N = p.n_patches;
   const int T = p.n_ktiles;
+  // Tiles of this block: blockIdx.x, blockIdx.x + gridDim.x, ... (the grid
+  // has at most n_tiles blocks, so every block has at least one).
+  const int n_mine = (p.n_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                     static_cast<int>(gridDim.x);
+  auto tile_of = [&](int i) -> int { return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x); };
+  auto tile_bh = [&](int i) -> int { return tile_of(i) / p.n_qblocks; };
+  auto tile_row0 = [&](int i) -> int { return (tile_of(i) % p.n_qblocks) * (kBM * NQ); };
 
-  // S buffer of query tile t for key tile j, and the phase of its barriers
-  auto sbuf = [](int t, int j) -> int { return NQ == 2 ? t : (j & 1); };
-  auto sphase = [](int j) -> uint32_t {
-    return NQ == 2 ? (static_cast<uint32_t>(j) & 1u) : (static_cast<uint32_t>(j >> 1) & 1u);
+  // Key tiles are numbered across the tiles of the block (g = i * T + j), so
+  // every ring of barriers keeps its phase from one tile to the next.
+  // S buffer of query tile t for key tile g, and the phase of its barriers
+  auto sbuf = [](int t, int64_t g) -> int { return NQ == 2 ? t : static_cast<int>(g & 1); };
+  auto sphase = [](int64_t g) -> uint32_t {
+    return NQ == 2 ? static_cast<uint32_t>(g & 1) : static_cast<uint32_t>((g >> 1) & 1);
   };
-  // barrier telling that the S buffer of key tile j was copied to registers
-  auto sfree_bar = [](int j) -> int { return NQ == 2 ? 0 : (j & 1); };
-  // K/V stage of key tile j and the phase of its barriers
-  auto kv_phase = [](int j) -> uint32_t { return static_cast<uint32_t>(j / S) & 1u; };
+  // barrier telling that the S buffer of key tile g was copied to registers
+  auto sfree_bar = [](int64_t g) -> int { return NQ == 2 ? 0 : static_cast<int>(g & 1); };
+  // K/V stage of key tile g and the phase of its barriers
+  auto kv_stage = [](int64_t g) -> int { return static_cast<int>(g % S); };
+  auto kv_phase = [](int64_t g) -> uint32_t { return static_cast<uint32_t>((g / S) & 1); };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(kBarQFull), 1);
+    ptx::mbar_init(bar(kBarQEmpty), 1);
     for (int i = 0; i < S; ++i) {
       ptx::mbar_init(bar(kBarKFull + i), 1);
       ptx::mbar_init(bar(kBarKEmpty + i), 1);
@@ -236,50 +258,65 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + P::kOffBar + kTmemSlotOff);
+  const uint32_t tile_bytes = static_cast<uint32_t>(P::kTileF16);
 
   const bool softmax_wg = warp >= 4;
   if (!softmax_wg) {
     if (P::kSplitRegs) ptx::regs_decrease<P::kRegsOther>();
     if (warp == 0) {
-      // ---------------------------------------------------------- producer
+      // ------------------------------------------------- K/V producer
+      // Runs ahead across tile boundaries: the next tile's first K/V tiles
+      // are in flight while the current one ends.
       if (lane == 0) {
-        ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
-        const uint32_t tile_bytes = static_cast<uint32_t>(P::kTileF16);
-        ptx::mbar_arrive_expect_tx(bar(kBarQFull), NQ * tile_bytes);
-        for (int t = 0; t < NQ; ++t)
-          for (int kb = 0; kb < NKB; ++kb)
-            ptx::tma_load_3d(base_s + P::kOffQ + t * P::kTileF16 + kb * kBoxBytes, &tm_q,
-                             bar(kBarQFull), kb * 64, q_row0 + t * kBM, bh);
-        int issued = 0;  // key tiles whose K and V loads were issued
-        for (int j = 0; j < T; ++j) {
-          const int st = j % S;
-          const uint32_t free_par = kv_phase(j) ^ 1u;
-          if (!w.wait(bar(kBarKEmpty + st), free_par, kSiteProducerK)) break;
-          ptx::mbar_arrive_expect_tx(bar(kBarKFull + st), tile_bytes);
-          for (int kb = 0; kb < NKB; ++kb)
-            ptx::tma_load_3d(base_s + P::kOffK + st * P::kTileF16 + kb * kBoxBytes, &tm_k,
-                             bar(kBarKFull + st), kb * 64, j * kBN, bh);
-          if (!w.wait(bar(kBarVEmpty + st), free_par, kSiteProducerV)) {
-            // keep the barrier accounting of the issued K load for the drain
-            issued = -(j + 1);
-            break;
+        int64_t k_issued = 0, v_issued = 0;
+        bool ok = true;
+        for (int i = 0; ok && i < n_mine; ++i) {
+          const int bh = tile_bh(i);
+          for (int j = 0; j < T; ++j) {
+            const int64_t g = static_cast<int64_t>(i) * T + j;
+            const int st = kv_stage(g);
+            const uint32_t free_par = kv_phase(g) ^ 1u;
+            if (!(ok = w.wait(bar(kBarKEmpty + st), free_par, kSiteProducerK))) break;
+            ptx::mbar_arrive_expect_tx(bar(kBarKFull + st), tile_bytes);
+            for (int kb = 0; kb < NKB; ++kb)
+              ptx::tma_load_3d(base_s + P::kOffK + st * P::kTileF16 + kb * kBoxBytes, &tm_k,
+                               bar(kBarKFull + st), kb * 64, j * kBN, bh);
+            ++k_issued;
+            if (!(ok = w.wait(bar(kBarVEmpty + st), free_par, kSiteProducerV))) break;
+            ptx::mbar_arrive_expect_tx(bar(kBarVFull + st), tile_bytes);
+            for (int kb = 0; kb < NKB; ++kb)
+              ptx::tma_load_3d(base_s + P::kOffV + st * P::kTileF16 + kb * kBoxBytes, &tm_v,
+                               bar(kBarVFull + st), kb * 64, j * kBN, bh);
+            ++v_issued;
           }
-          ptx::mbar_arrive_expect_tx(bar(kBarVFull + st), tile_bytes);
-          for (int kb = 0; kb < NKB; ++kb)
-            ptx::tma_load_3d(base_s + P::kOffV + st * P::kTileF16 + kb * kBoxBytes, &tm_v,
-                             bar(kBarVFull + st), kb * 64, j * kBN, bh);
-          issued = j + 1;
         }
         // every issued copy must have landed before the block exits
-        w.drain(bar(kBarQFull), 0, kSiteDrainTma);
-        const int k_loads = issued >= 0 ? issued : -issued;  // K loads issued
-        const int v_loads = issued >= 0 ? issued : -issued - 1;
-        for (int j = (k_loads > S ? k_loads - S : 0); j < k_loads; ++j)
-          w.drain(bar(kBarKFull + j % S), kv_phase(j), kSiteDrainTma);
-        for (int j = (v_loads > S ? v_loads - S : 0); j < v_loads; ++j)
-          w.drain(bar(kBarVFull + j % S), kv_phase(j), kSiteDrainTma);
+        for (int64_t g = (k_issued > S ? k_issued - S : 0); g < k_issued; ++g)
+          w.drain(bar(kBarKFull + kv_stage(g)), kv_phase(g), kSiteDrainTma);
+        for (int64_t g = (v_issued > S ? v_issued - S : 0); g < v_issued; ++g)
+          w.drain(bar(kBarVFull + kv_stage(g)), kv_phase(g), kSiteDrainTma);
+      }
+    } else if (warp == 3) {
+      // --------------------------------------------------- Q producer
+      // The Q tiles of tile i go in as soon as the S products of tile i-1
+      // have read the previous ones.
+      if (lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        int q_issued = 0;
+        for (int i = 0; i < n_mine; ++i) {
+          if (i > 0 && !w.wait(bar(kBarQEmpty), static_cast<uint32_t>(i - 1) & 1u, kSiteProducerQ))
+            break;
+          ptx::mbar_arrive_expect_tx(bar(kBarQFull), NQ * tile_bytes);
+          for (int t = 0; t < NQ; ++t)
+            for (int kb = 0; kb < NKB; ++kb)
+              ptx::tma_load_3d(base_s + P::kOffQ + t * P::kTileF16 + kb * kBoxBytes, &tm_q,
+                               bar(kBarQFull), kb * 64, tile_row0(i) + t * kBM, tile_bh(i));
+          ++q_issued;
+        }
+        if (q_issued > 0)
+          w.drain(bar(kBarQFull), static_cast<uint32_t>(q_issued - 1) & 1u, kSiteDrainTma);
       }
     } else if (warp == 1 || warp == 2) {
       // ---------------------------------------------------------- MMA issuers
@@ -287,62 +324,67 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
       // having copied S out, the P V products on P being written, and on
       // nothing else of each other, so each issuer waits once per key tile.
       if (lane == 0 && warp == 1) {
-        // S(t, j) = Q_t K_j^T into S buffer sbuf(t, j)
+        // S(t, g) = Q_t K_g^T into S buffer sbuf(t, g)
         const uint32_t idesc_s = ptx::idesc_f16_f32(kBM, kBN, false);
         const int ksteps = p.d_pad >> 4;
-        auto issue_s = [&](int t, int j) {
+        auto issue_s = [&](int t, int64_t g) {
           const uint32_t qa = base_s + P::kOffQ + t * P::kTileF16;
-          const uint32_t kb = base_s + P::kOffK + (j % S) * P::kTileF16;
-          const uint32_t d = tmem + static_cast<uint32_t>(sbuf(t, j)) * 128u;
+          const uint32_t kb = base_s + P::kOffK + kv_stage(g) * P::kTileF16;
+          const uint32_t d = tmem + static_cast<uint32_t>(sbuf(t, g)) * 128u;
           for (int ks = 0; ks < ksteps; ++ks) {
             const uint32_t off = static_cast<uint32_t>((ks >> 2) * kBoxBytes + (ks & 3) * 32);
             ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
                         ptx::smem_desc(kb + off, 16, 1024, ptx::kSwizzle128B), idesc_s,
                         ks > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(bar(kBarSFull + sbuf(t, j)));
+          ptx::mma_commit(bar(kBarSFull + sbuf(t, g)));
         };
-        bool ok = w.wait(bar(kBarQFull), 0, kSiteMmaQ) && w.wait(bar(kBarKFull), 0, kSiteMmaK);
-        if (ok) {
-          ptx::tc_fence_after();
-          for (int t = 0; t < NQ; ++t) issue_s(t, 0);
-          ptx::mma_commit(bar(kBarKEmpty));
-        }
-        for (int j = 0; ok && j + 1 < T; ++j) {
-          // S of key tile j+1 needs K_{j+1} and the softmax to have copied
-          // the previous contents of its buffer(s) to registers
-          const int nst = (j + 1) % S;
-          if (!(ok = w.wait(bar(kBarKFull + nst), kv_phase(j + 1), kSiteMmaK))) break;
-          const int prev = NQ == 2 ? j : j - 1;  // last key tile that used the buffer(s)
-          if (prev >= 0 &&
-              !(ok = w.wait(bar(kBarSFree + sfree_bar(prev)), sphase(prev), kSiteMmaSFree)))
-            break;
-          ptx::tc_fence_after();
-          for (int t = 0; t < NQ; ++t) issue_s(t, j + 1);
-          ptx::mma_commit(bar(kBarKEmpty + nst));
+        bool ok = true;
+        for (int i = 0; ok && i < n_mine; ++i) {
+          if (!(ok = w.wait(bar(kBarQFull), static_cast<uint32_t>(i) & 1u, kSiteMmaQ))) break;
+          for (int j = 0; j < T; ++j) {
+            const int64_t g = static_cast<int64_t>(i) * T + j;
+            // S of key tile g needs K_g and the softmax to have copied the
+            // previous contents of its buffer(s) to registers
+            if (!(ok = w.wait(bar(kBarKFull + kv_stage(g)), kv_phase(g), kSiteMmaK))) break;
+            const int64_t prev = NQ == 2 ? g - 1 : g - 2;  // last key tile that used the buffer(s)
+            if (prev >= 0 &&
+                !(ok = w.wait(bar(kBarSFree + sfree_bar(prev)), sphase(prev), kSiteMmaSFree)))
+              break;
+            ptx::tc_fence_after();
+            for (int t = 0; t < NQ; ++t) issue_s(t, g);
+            ptx::mma_commit(bar(kBarKEmpty + kv_stage(g)));
+          }
+          // the Q tiles are free once these S products have run
+          if (ok) ptx::mma_commit(bar(kBarQEmpty));
         }
         ptx::mma_commit(bar(kBarMmaDone));
       } else if (lane == 0 && warp == 2) {
-        // O_t += P_t V_j
+        // O_t += P_t V_g
         const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
-        auto issue_pv = [&](int t, int j) {
-          const uint32_t vb = base_s + P::kOffV + (j % S) * P::kTileF16;
+        auto issue_pv = [&](int t, int64_t g, bool first) {
+          const uint32_t vb = base_s + P::kOffV + kv_stage(g) * P::kTileF16;
           const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
           const uint32_t a = tmem + P::kColP + static_cast<uint32_t>(t) * P::kColStride;
           for (int ks = 0; ks < kBN / 16; ++ks) {
             ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
                         ptx::smem_desc(vb + ks * 2048, kBoxBytes, 1024, ptx::kSwizzle128B),
-                        idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+                        idesc_pv, (!first || ks > 0) ? 1u : 0u);
           }
           ptx::mma_commit(bar(kBarODone + t));
         };
         bool ok = true;
-        for (int j = 0; ok && j < T; ++j) {
-          if (!(ok = w.wait(bar(kBarVFull + j % S), kv_phase(j), kSiteMmaV))) break;
-          if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(j) & 1u, kSiteMmaP))) break;
-          ptx::tc_fence_after();
-          for (int t = 0; t < NQ; ++t) issue_pv(t, j);
-          ptx::mma_commit(bar(kBarVEmpty + j % S));
+        for (int i = 0; ok && i < n_mine; ++i) {
+          for (int j = 0; j < T; ++j) {
+            const int64_t g = static_cast<int64_t>(i) * T + j;
+            if (!(ok = w.wait(bar(kBarVFull + kv_stage(g)), kv_phase(g), kSiteMmaV))) break;
+            // P of key tile g written (for the first key tile of a tile this
+            // also tells that the softmax has read the previous tile's O)
+            if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
+            ptx::tc_fence_after();
+            for (int t = 0; t < NQ; ++t) issue_pv(t, g, j == 0);
+            ptx::mma_commit(bar(kBarVEmpty + kv_stage(g)));
+          }
         }
         ptx::mma_commit(bar(kBarMmaDone));
       }
@@ -355,101 +397,145 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t p_addr = tmem + lane_addr + P::kColP + static_cast<uint32_t>(t) * P::kColStride;
     const uint32_t o_addr = tmem + lane_addr + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
-    float m_ref = -INFINITY;  // running max in log2 units (may lag the true max by < 8)
-    float l = 0.0f;           // running sum of exp2(s*log2e - m_ref)
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int buf = sbuf(t, j);
-      if (!(ok = w.wait_warp(bar(kBarSFull + buf), sphase(j), kSiteSoftS))) break;
-      ptx::tc_fence_after();
-      const uint32_t s_addr = tmem + lane_addr + static_cast<uint32_t>(buf) * 128u;
-      const int valid = N - j * kBN;
-
-      // the whole S row (128 columns) into registers, one wait; then the
-      // buffer is released for the next S = Q K^T
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(s_addr + c * 32, r[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld_dep(r[c]);
-      ptx::tc_fence_before();
-      warp_arrive(bar(kBarSFree + sfree_bar(j)));
-
-      if (valid < kBN) {  // ragged last key tile only: keys >= n_patches score -inf
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= valid) r[c][i] = 0xff800000u;
-      }
-      float mc[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float a = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 32; i += 2)
-          a = ptx::max3(a, __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
-        mc[c] = a;
-      }
-      const float mt = ptx::max3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * kLog2e;
-      const bool need = mt > m_ref + kRescaleLog2;
-      const float m_new = need ? mt : m_ref;
-      const float alpha = ptx::ex2_approx(m_ref - m_new);  // 0 on the first tile, 1 if kept
-      m_ref = m_new;
-
-      // p = 2^(s*log2e - m_ref) as f16 pairs, kept in registers: the P
-      // buffer may still be read by the previous key tile's P V, which runs
-      // on the tensor core meanwhile
-      const float2 scale = make_float2(kLog2e, kLog2e);
-      const float2 shift = make_float2(-m_ref, -m_ref);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-      uint32_t pk[4][16];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x = __ffma2_rn(
-              make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), scale,
-              shift);
-          const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-          acc[i & 3] = __fadd2_rn(acc[i & 3], pp);
-          pk[c][i] = ptx::pack_half2(pp.x, pp.y);
-        }
-      }
-      const float2 s01 = __fadd2_rn(acc[0], acc[1]);
-      const float2 s23 = __fadd2_rn(acc[2], acc[3]);
-      l = fmaf(l, alpha, (s01.x + s01.y) + (s23.x + s23.y));
-      if (j > 0) {
-        // P V of the previous key tile has finished: P buffer free, O final
-        if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(j - 1) & 1u,
-                               kSiteSoftO)))
-          break;
+    for (int i = 0; ok && i < n_mine; ++i) {
+      float m_ref = -INFINITY;  // running max in log2 units (may lag the true max by < 8)
+      float l = 0.0f;           // running sum of exp2(s*log2e - m_ref)
+      int64_t g = static_cast<int64_t>(i) * T;
+      for (int j = 0; j < T; ++j, ++g) {
+        const int buf = sbuf(t, g);
+        if (!(ok = w.wait_warp(bar(kBarSFull + buf), sphase(g), kSiteSoftS))) break;
         ptx::tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-          for (int c = 0; c < (p.d_pad >> 4); ++c) {
-            uint32_t y[16];
-            ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
-            ptx::tmem_wait_ld_dep16(y);
+        const uint32_t s_addr = tmem + lane_addr + static_cast<uint32_t>(buf) * 128u;
+        const int valid = N - j * kBN;
+
+        // the whole S row (128 columns) into registers, one wait; then the
+        // buffer is released for the next S = Q K^T
+        uint32_t r[4][32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
-            ptx::tmem_st_32x32b_x16(o_addr + c * 16, y);
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(s_addr + c * 32, r[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_wait_ld_dep(r[c]);
+        ptx::tc_fence_before();
+        warp_arrive(bar(kBarSFree + sfree_bar(g)));
+
+        if (valid < kBN) {  // ragged last key tile only: keys >= n_patches score -inf
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e >= valid) r[c][e] = 0xff800000u;
+        }
+        float mc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float a = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            a = ptx::max3(a, __uint_as_float(r[c][e]), __uint_as_float(r[c][e + 1]));
+          mc[c] = a;
+        }
+        const float mt = ptx::max3(mc[0], mc[1], fmaxf(mc[2], mc[3])) * kLog2e;
+        const bool need = mt > m_ref + kRescaleLog2;
+        const float m_new = need ? mt : m_ref;
+        const float alpha = ptx::ex2_approx(m_ref - m_new);  // 0 on the first key tile, 1 if kept
+        m_ref = m_new;
+
+        // p = 2^(s*log2e - m_ref) as f16 pairs, kept in registers: the P
+        // buffer may still be read by the previous key tile's P V, which
+        // runs on the tensor core meanwhile
+        const float2 scale = make_float2(kLog2e, kLog2e);
+        const float2 shift = make_float2(-m_ref, -m_ref);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        uint32_t pk[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(r[c][2 * e]), __uint_as_float(r[c][2 * e + 1])), scale,
+                shift);
+            const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+            acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
+            pk[c][e] = ptx::pack_half2(pp.x, pp.y);
           }
         }
-      }
+        const float2 s01 = __fadd2_rn(acc[0], acc[1]);
+        const float2 s23 = __fadd2_rn(acc[2], acc[3]);
+        l = fmaf(l, alpha, (s01.x + s01.y) + (s23.x + s23.y));
+        if (j > 0) {
+          // P V of the previous key tile has finished: P buffer free, O final.
+          // (For j == 0 the previous tile's epilogue already waited for it.)
+          if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>((g - 1) & 1),
+                                 kSiteSoftO)))
+            break;
+          ptx::tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+            for (int c = 0; c < (p.d_pad >> 4); ++c) {
+              uint32_t y[16];
+              ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
+              ptx::tmem_wait_ld_dep16(y);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk[c]);
+              for (int e = 0; e < 16; ++e) y[e] = __float_as_uint(__uint_as_float(y[e]) * alpha);
+              ptx::tmem_st_32x32b_x16(o_addr + c * 16, y);
+            }
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk[c]);
 
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      warp_arrive(bar(kBarPFull));
-    }
-    if (ok && w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>(T - 1) & 1u, kSiteEpilogue)) {
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        warp_arrive(bar(kBarPFull));
+      }
+      if (!ok) break;
+      // ---- epilogue of the tile: out = O / l for the rows < n_patches.  The
+      // next tile's first P V overwrites O only after this warp's next P
+      // arrival, which follows these reads.
+      if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>((g - 1) & 1),
+                             kSiteEpilogue)))
+        break;
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
-      const int row = q_row0 + t * kBM + quarter * 32 + lane;
+      if (NKB == 1 && p.tma_out) {
+        // 16 columns at a time: TMEM -> registers -> swizzled shared buffer
+        // -> one TMA store of the warp's 32 rows (rows past n_patches and
+        // columns past head_dim are not written); the stores complete in
+        // the background while the warp moves on to the next tile
+        const uint32_t epi =
+            base_s + P::kOffEpi + static_cast<uint32_t>(warp - 4) * 4096u;
+        const int row_base = tile_row0(i) + t * kBM + quarter * 32;
+        for (int c = 0; c < (p.d_pad >> 4); ++c) {
+          uint32_t y[16];
+          ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
+          // buffer c & 1 is free once the store issued two chunks earlier
+          // (of this tile or the previous one) has read it
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
+          ptx::tmem_wait_ld_dep16(y);
+          const uint32_t buf = epi + static_cast<uint32_t>(c & 1) * 2048u;
+          const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(k) ^ ((lane >> 1) & 3u)) << 4),
+                              __uint_as_float(y[4 * k + 0]) * inv_l,
+                              __uint_as_float(y[4 * k + 1]) * inv_l,
+                              __uint_as_float(y[4 * k + 2]) * inv_l,
+                              __uint_as_float(y[4 * k + 3]) * inv_l);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tm_o, buf, c * 16, row_base, tile_bh(i));
+            ptx::bulk_commit_group();
+          }
+        }
+        ptx::tc_fence_before();
+        continue;
+      }
+      const int row = tile_row0(i) + t * kBM + quarter * 32 + lane;
       const int D = p.head_dim;
-      float* orow = p.out + (static_cast<size_t>(bh) * N + row) * D;
+      float* orow = p.out + (static_cast<size_t>(tile_bh(i)) * N + row) * D;
       for (int c = 0; c < (p.d_pad >> 4); ++c) {
         uint32_t y[16];
         ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
@@ -470,14 +556,17 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int d = c * 16 + i;
-              if (d < D) orow[d] = __uint_as_float(y[i]) * inv_l;
+            for (int e = 0; e < 16; ++e) {
+              const int d = c * 16 + e;
+              if (d < D) orow[d] = __uint_as_float(y[e]) * inv_l;
             }
           }
         }
       }
+      ptx::tc_fence_before();
     }
+    // the output stores must have completed before the block exits
+    if (NKB == 1 && p.tma_out && lane == 0) ptx::bulk_wait_group_all();
   }
 
   ptx::tc_fence_before();

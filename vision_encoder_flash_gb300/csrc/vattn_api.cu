@@ -85,6 +85,30 @@ vattn_status make_tmap16(CUtensorMap* tm, const __half* ptr, int64_t bh, int64_t
   return VATTN_OK;
 }
 
+// 3-D view {head_dim, n_patches, batch*n_heads} of the f32 output for the
+// kernel's TMA stores: box = 32 rows x 16 columns (64 bytes), 64-byte swizzle
+// (the layout the kernel writes to its staging buffers).  Needs head_dim % 4
+// == 0 and a 16-byte aligned base.
+vattn_status make_tmap_out(CUtensorMap* tm, float* out, int64_t bh, int64_t n, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    if (g_encode_err != cudaSuccess) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
+    return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                              static_cast<cuuint64_t>(bh)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4u,
+                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(d) * 4u};
+  const cuuint32_t box[3] = {16u, 32u, 1u};
+  const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box,
+                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled (out) failed with CUresult %d", static_cast<int>(r));
+  return VATTN_OK;
+}
+
 constexpr int kMaxDevices = 64;
 
 // Per-device memory pool for the f16 staging workspace: stream-ordered
@@ -115,9 +139,26 @@ vattn_status pool_for(int device, cudaMemPool_t* out) {
   return VATTN_OK;
 }
 
+// Streaming multiprocessors of a device, looked up once per device.
+std::atomic<int> g_sm_count[kMaxDevices];
+
+vattn_status sm_count(int device, int* out) {
+  int n = g_sm_count[device].load(std::memory_order_acquire);
+  if (n <= 0) {
+    const cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(multiprocessor count)");
+    if (n <= 0) return fail(VATTN_ERR_CUDA, "device reports %d multiprocessors", n);
+    g_sm_count[device].store(n, std::memory_order_release);
+  }
+  *out = n;
+  return VATTN_OK;
+}
+
+// The attention kernel is persistent: one block per multiprocessor (at most
+// one per tile), each looping over the tiles blockIdx.x + k * gridDim.x.
 template <int NQ, int NKB>
 vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const vattn::Params& p, unsigned grid, cudaStream_t stream,
+                              vattn::Params p, unsigned n_tiles, cudaStream_t stream,
                               int device) {
   using P = vattn::Plan<NQ, NKB>;
   auto kernel = vattn::vattn_fwd_kernel<NQ, NKB>;
@@ -128,7 +169,22 @@ vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, cons
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     configured[device].store(1, std::memory_order_release);
   }
-  kernel<<<grid, P::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, p);
+  int sms = 0;
+  const vattn_status st = sm_count(device, &sms);
+  if (st != VATTN_OK) return st;
+  const unsigned grid = n_tiles < static_cast<unsigned>(sms) ? n_tiles : static_cast<unsigned>(sms);
+  // the output goes through TMA stores when the kernel variant stages it
+  // (head_dim <= 64) and its rows are whole 16-byte units
+  CUtensorMap to;
+  std::memset(&to, 0, sizeof(to));
+  p.tma_out = 0;
+  if (NKB == 1 && p.vec_out) {
+    const vattn_status so = make_tmap_out(&to, p.out, static_cast<int64_t>(p.n_tiles / p.n_qblocks),
+                                          p.n_patches, p.head_dim);
+    if (so != VATTN_OK) return so;
+    p.tma_out = 1;
+  }
+  kernel<<<grid, P::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   return VATTN_OK;
@@ -191,6 +247,7 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   p.head_dim = D;
   p.d_pad = d_pad;
   p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
   p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
   p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
 
@@ -295,6 +352,7 @@ vattn_status vattn_forward_f16(const uint16_t* q, const uint16_t* k, const uint1
   p.head_dim = D;
   p.d_pad = d_pad;
   p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
   p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
   p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
 
@@ -449,6 +507,7 @@ extern "C" vattn_status vattn_forward_noalloc(const float* q, const float* k, co
   p.head_dim = D;
   p.d_pad = d_pad;
   p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
   p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
   p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
 
