@@ -8,6 +8,9 @@ It restates, in plain f64 C (``vattn_oracle.c``), what the WGSL shader
 ``out[b, h, i, :] = softmax_j(q[b,h,i,:] . k[b,h,j,:]) @ v[b,h,:,:]`` with no
 1/sqrt(head_dim) factor (q arrives pre-scaled), head-major layout
 ``[batch, n_heads, n_patches, head_dim]``.
+
+``oracle.rope`` (plain NumPy, f64) restates the NeoX rotary embedding of the
+WGSL kernel "rope_neox_backward.wgsl" (rullama 0.2.0), forward and inverse.
 """
 from __future__ import annotations
 
