@@ -422,6 +422,44 @@ def run_vattn(args, workload):
         if vef.device_status() != 0:
             raise RuntimeError("kernel reported a wait timeout")
 
+    # ---- NeoX RoPE rows (context): the rotation fused into the staging pass
+    # of a full call, and the standalone in-place rotation of q (HBM-bound:
+    # every rotated f32 element read and written once)
+    variants = {}
+    if not args.no_extras:
+        reps = 200
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(10):
+            vef.forward_rope(qd, kd, vd, D, 0, 10000.0, out=out)
+        a.record(stream)
+        for _ in range(reps):
+            vef.forward_rope(qd, kd, vd, D, 0, 10000.0, out=out)
+        b2.record(stream)
+        torch.cuda.synchronize(dev)
+        fms = a.elapsed_time(b2) / reps
+        xr = torch.cat([qd, kd, vd], dim=0)  # 226 MB > L2: every step streams from HBM
+        for _ in range(10):
+            vef.rope_neox(xr, D, 0, 10000.0)
+        a.record(stream)
+        for _ in range(reps):
+            vef.rope_neox(xr, D, 0, 10000.0)
+        b2.record(stream)
+        torch.cuda.synchronize(dev)
+        rms = a.elapsed_time(b2) / reps
+        rbytes = 3 * B * H * N * (D // 2 * 2) * 4 * 2
+        if vef.device_status() != 0:
+            raise RuntimeError("kernel reported a wait timeout")
+        variants = {
+            "rope_fused_call": {"ms": round(fms, 5), "tflops": round(flops / fms / 1e9, 2),
+                                "vs_plain_call": round(fms / ms_per_step, 4),
+                                "what": "vattn_forward_rope, rope_dims = head_dim, pos0 0, base 1e4"},
+            "rope_inplace": {"ms": round(rms, 5), "bytes": rbytes,
+                             "achieved_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1),
+                             "frac_of_hbm": round(rbytes / (rms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4),
+                             "what": "vattn_rope_neox on q, k, v stacked (f32, in place, 226 MB > L2), includes the angle-table kernel"},
+        }
+        del xr
+
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()
@@ -455,6 +493,7 @@ def run_vattn(args, workload):
                 "path": "vision_encoder_flash_gb300.forward on pinned host tensors"},
         "gpu_launches": 2 * args.steps,  # staging kernel + attention kernel per step
         "other_workloads": extras,
+        "variants": variants,
     }
     print(json.dumps(line), flush=True)
     if pg is not None:

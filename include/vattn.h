@@ -101,6 +101,49 @@ vattn_status vattn_forward_f16(const uint16_t* q, const uint16_t* k, const uint1
                                int64_t head_dim, void* stream);
 
 /*
+ * vattn_rope_neox -- NeoX rotary position embedding, in place.
+ *
+ * The rotation of the WGSL kernel "rope_neox_backward.wgsl" (rullama 0.2.0):
+ * with half = rope_dims / 2, in every row the pair (x[i], x[i + half]),
+ * i < half, is turned by theta_i = pos * base^(-2 i / rope_dims), divided by
+ * factors[i] when factors is not NULL:
+ *   inverse == 0 (forward): x[i] <- a cos - b sin,  x[i + half] <- a sin + b cos
+ *   inverse == 1 (backward): x[i] <- a cos + b sin, x[i + half] <- -a sin + b cos
+ * with a = x[i], b = x[i + half]; dims >= 2 * half are not touched.  theta,
+ * cos and sin are computed in f32 as on the page (f32(pos) * pow(base,
+ * -2 i / rope_dims), then / factors[i]).
+ *
+ * x: DEVICE pointer to a contiguous f32 tensor [batch, n_heads, n_patches,
+ *   head_dim] (head-major, 4-byte aligned); patch n is at position
+ *   pos0 + n.  (With n_patches == 1 and pos0 == pos this is the page's
+ *   kernel on [n_heads, head_dim].)
+ * rope_dims: 0..head_dim (odd values leave dim rope_dims - 1 alone, as the
+ *   page's integer half does); base: finite, > 0; pos0 >= 0 with
+ *   pos0 + n_patches <= 2^24 (positions exact in f32); factors: NULL or a
+ *   DEVICE pointer to rope_dims / 2 floats.
+ * Asynchronous on `stream`; a small angle table (n_patches * rope_dims / 2
+ * * 8 bytes) is taken stream-ordered from the library's memory pool.
+ * Argument errors are returned before any CUDA call.
+ */
+vattn_status vattn_rope_neox(float* x, int64_t batch, int64_t n_heads, int64_t n_patches,
+                             int64_t head_dim, int64_t rope_dims, int64_t pos0, float base,
+                             const float* factors, int inverse, void* stream);
+
+/*
+ * vattn_forward_rope -- vattn_forward on q and k turned by the forward NeoX
+ * rotation of vattn_rope_neox (patch n at position pos0 + n), fused into the
+ * f16 staging pass: q and k are read once, rotated in f32 and rounded to f16;
+ * the caller's q and k are not modified.  The rotation is the one the page
+ * "rope_neox_backward.wgsl" applies around attention; the attention is that
+ * of vattn_forward.  Arguments and errors: those of vattn_forward and of
+ * vattn_rope_neox.  Workspace: vattn_forward's plus the angle table.
+ */
+vattn_status vattn_forward_rope(const float* q, const float* k, const float* v, float* out,
+                                int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, int64_t rope_dims, int64_t pos0, float base,
+                                const float* factors, void* stream);
+
+/*
  * Size of the fixed staging scratch of vattn_forward_noalloc: 32 MiB, enough
  * for batch*n_heads*n_patches*round_up(head_dim, 16) <= 5,592,320 (for
  * example 16 heads x 4,100 patches at head_dim 72, or 64 heads x 1,024

@@ -19,6 +19,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = _lib.exported_symbols()
     assert set(names) == {"vattn_forward", "vattn_forward_f16", "vattn_forward_noalloc",
+                          "vattn_rope_neox", "vattn_forward_rope",
                           "vattn_device_status", "vattn_status_string",
                           "vattn_last_error_string", "vattn_version"}
     for name in names:
@@ -136,3 +137,52 @@ def test_device_status_without_gpu_reports_cuda_error(lib):
     code = ctypes.c_uint32(7)
     assert lib.vattn_device_status(ctypes.byref(code)) == 4
     assert code.value == 0
+
+
+# vattn_rope_neox(x, B, H, N, D, rope_dims, pos0, base, factors, inverse)
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, -1, 2, 3, 8, 8, 0, 1e4, 0, 0), 1),
+    ((FAKE, 1, 2, 3, 0, 0, 0, 1e4, 0, 0), 1),           # head_dim 0
+    ((FAKE, 1, 2, 3, 8, 10, 0, 1e4, 0, 0), 1),          # rope_dims > head_dim
+    ((FAKE, 1, 2, 3, 8, -2, 0, 1e4, 0, 0), 1),
+    ((FAKE, 1, 2, 3, 8, 8, 0, 0.0, 0, 0), 1),           # base must be > 0
+    ((FAKE, 1, 2, 3, 8, 8, 0, -2.0, 0, 0), 1),
+    ((FAKE, 1, 2, 3, 8, 8, 0, float("nan"), 0, 0), 1),
+    ((FAKE, 1, 2, 3, 8, 8, 0, float("inf"), 0, 0), 1),
+    ((FAKE, 1, 2, 3, 8, 8, -1, 1e4, 0, 0), 1),          # pos0 < 0
+    ((FAKE, 1, 2, 3, 8, 8, 2 ** 24 - 2, 1e4, 0, 0), 2),  # last position past 2^24
+    ((FAKE, 1, 2, 3, 8, 8, 0, 1e4, 0, 2), 1),           # inverse must be 0 or 1
+    ((FAKE + 2, 1, 2, 3, 8, 8, 0, 1e4, 0, 0), 3),
+    ((FAKE, 1, 2, 3, 8, 8, 0, 1e4, FAKE + 1, 0), 3),    # misaligned factors
+    ((0, 1, 2, 3, 8, 8, 0, 1e4, 0, 0), 1),              # null x
+])
+def test_rope_host_side_argument_errors(lib, args, status):
+    assert _lib.rope_neox_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""
+
+
+@pytest.mark.parametrize("args", [
+    (0, 0, 2, 3, 8, 8, 0, 1e4, 0, 0),       # no batch
+    (0, 1, 2, 0, 8, 8, 0, 1e4, 0, 0),       # no patches
+    (0, 1, 2, 3, 8, 0, 0, 1e4, 0, 0),       # rope_dims 0: nothing turns
+    (0, 1, 2, 3, 8, 1, 0, 1e4, 0, 0),       # rope_dims 1: half = 0
+])
+def test_rope_no_ops_need_no_pointer(lib, args):
+    assert _lib.rope_neox_status(*args, 0) == 0
+
+
+# vattn_forward_rope(q, k, v, out, B, H, N, D, rope_dims, pos0, base, factors)
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8, 9, 0, 1e4, 0), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8, 8, 0, -1.0, 0), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8, 8, -5, 1e4, 0), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 136, 8, 0, 1e4, 0), 2),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8, 8, 2 ** 24, 1e4, 0), 2),
+    ((FAKE + 2, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8, 8, 0, 1e4, 0), 3),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8, 8, 0, 1e4, FAKE + 2), 3),
+    ((FAKE, FAKE, FAKE, FAKE + 4, 1, 2, 3, 8, 8, 0, 1e4, 0), 1),   # out overlaps q
+    ((FAKE, FAKE, FAKE, 0, 1, 2, 3, 8, 8, 0, 1e4, 0), 1),
+])
+def test_forward_rope_host_side_argument_errors(lib, args, status):
+    assert _lib.forward_rope_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""

@@ -9,11 +9,12 @@ missing or no GPU is present the calls raise.
 """
 from __future__ import annotations
 
-from ._lib import (VattnError, device_status, exported_symbols, forward_f16_raw,
-                   forward_noalloc_raw, forward_raw, lib_path, load_library, status_string,
-                   version)
+from ._lib import (VattnError, _check, device_status, exported_symbols, forward_f16_raw,
+                   forward_noalloc_raw, forward_raw, forward_rope_status, lib_path,
+                   load_library, rope_neox_status, status_string, version)
 
-__all__ = ["forward", "forward_f16", "forward_raw", "forward_f16_raw", "forward_noalloc_raw",
+__all__ = ["forward", "forward_f16", "forward_rope", "rope_neox", "forward_raw",
+           "forward_f16_raw", "forward_noalloc_raw",
            "device_status", "VattnError", "load_library",
            "lib_path", "exported_symbols", "status_string", "version"]
 
@@ -95,6 +96,69 @@ def forward_f16(q, k, v, out=None, stream=None):
     B, H, N, D = q.shape
     forward_f16_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D,
                     s.cuda_stream)
+    return out
+
+
+def _cuda_f32(name, t):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _factors_ptr(factors, rope_dims, device):
+    if factors is None:
+        return 0
+    _cuda_f32("factors", factors)
+    if factors.device != device or factors.numel() < rope_dims // 2:
+        raise ValueError("factors must hold rope_dims // 2 floats on the tensors' device")
+    return factors.data_ptr()
+
+
+def rope_neox(x, rope_dims, pos0=0, base=10000.0, factors=None, inverse=False, stream=None):
+    """NeoX rotary embedding of a CUDA f32 tensor ``[B, H, N, D]`` in place
+    (patch n at position ``pos0 + n``); ``inverse=True`` turns back.
+    Returns ``x`` without synchronising."""
+    import torch
+
+    _cuda_f32("x", x)
+    if x.dim() != 4:
+        raise ValueError("x must be [batch, n_heads, n_patches, head_dim]")
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    B, H, N, D = x.shape
+    _check(rope_neox_status(x.data_ptr(), B, H, N, D, rope_dims, pos0, float(base),
+                            _factors_ptr(factors, rope_dims, x.device), bool(inverse),
+                            s.cuda_stream))
+    return x
+
+
+def forward_rope(q, k, v, rope_dims, pos0=0, base=10000.0, factors=None, out=None, stream=None):
+    """out = softmax(rope(q) rope(k)^T) v for CUDA f32 tensors ``[B, H, N, D]``,
+    with the forward NeoX rotation of q and k (patch n at position ``pos0 + n``)
+    fused into the f16 staging; q and k are not modified."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_f32(name, t)
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [batch, n_heads, n_patches, head_dim]")
+    if not (q.shape == k.shape == v.shape) or not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must have one shape and one device")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_f32("out", out)
+    if out.shape != q.shape or out.device != q.device:
+        raise ValueError("out must match q in shape and device")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    B, H, N, D = q.shape
+    _check(forward_rope_status(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N,
+                               D, rope_dims, pos0, float(base),
+                               _factors_ptr(factors, rope_dims, q.device), s.cuda_stream))
     return out
 
 

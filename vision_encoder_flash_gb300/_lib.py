@@ -38,6 +38,11 @@ def load_library():
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.vattn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    lib.vattn_rope_neox.argtypes = [vp, i64, i64, i64, i64, i64, i64, f32, vp, ctypes.c_int, vp]
+    lib.vattn_rope_neox.restype = ctypes.c_int
+    lib.vattn_forward_rope.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp]
+    lib.vattn_forward_rope.restype = ctypes.c_int
     lib.vattn_forward_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_f16.restype = ctypes.c_int
     lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
@@ -86,6 +91,22 @@ def forward_f16_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, 
     """Like forward_f16_raw but returns the status code instead of raising."""
     return int(load_library().vattn_forward_f16(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                                 n_patches, head_dim, stream))
+
+
+def rope_neox_status(x_ptr, batch, n_heads, n_patches, head_dim, rope_dims, pos0, base,
+                     factors_ptr, inverse, stream=0) -> int:
+    """vattn_rope_neox with device addresses; returns the status code."""
+    return int(load_library().vattn_rope_neox(x_ptr, batch, n_heads, n_patches, head_dim,
+                                              rope_dims, pos0, base, factors_ptr, int(inverse),
+                                              stream))
+
+
+def forward_rope_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,
+                        rope_dims, pos0, base, factors_ptr, stream=0) -> int:
+    """vattn_forward_rope with device addresses; returns the status code."""
+    return int(load_library().vattn_forward_rope(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                                 n_patches, head_dim, rope_dims, pos0, base,
+                                                 factors_ptr, stream))
 
 
 def forward_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int,

@@ -19,6 +19,7 @@
 
 #include "../../include/vattn.h"
 #include "attn_kernel.cuh"
+#include "rope_kernel.cuh"
 #include "stage_kernel.cuh"
 
 namespace {
@@ -187,6 +188,23 @@ vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, cons
   kernel<<<grid, P::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+  return VATTN_OK;
+}
+
+// Arguments of the NeoX rotation (checked on the host, before any CUDA call).
+vattn_status check_rope(int64_t head_dim, int64_t n_patches, int64_t rope_dims, int64_t pos0,
+                        float base, const float* factors) {
+  if (rope_dims < 0 || rope_dims > head_dim)
+    return fail(VATTN_ERR_INVALID_ARG, "rope_dims %lld outside [0, head_dim = %lld]",
+                (long long)rope_dims, (long long)head_dim);
+  if (!(base > 0.0f) || base > 3.4e38f)
+    return fail(VATTN_ERR_INVALID_ARG, "base must be a finite positive number");
+  if (pos0 < 0) return fail(VATTN_ERR_INVALID_ARG, "pos0 must be >= 0");
+  if (pos0 > (int64_t{1} << 24) - n_patches)
+    return fail(VATTN_ERR_UNSUPPORTED,
+                "positions up to pos0 + n_patches - 1 must be exact in f32 (< 2^24)");
+  if (reinterpret_cast<uintptr_t>(factors) & 3u)
+    return fail(VATTN_ERR_MISALIGNED, "factors must be 4-byte aligned");
   return VATTN_OK;
 }
 
@@ -372,6 +390,173 @@ vattn_status vattn_forward_f16(const uint16_t* q, const uint16_t* k, const uint1
   if (nkb == 1 && nq == 2) return launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
   if (nkb == 1) return launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
   return launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+}
+
+vattn_status vattn_rope_neox(float* x, int64_t batch, int64_t n_heads, int64_t n_patches,
+                             int64_t head_dim, int64_t rope_dims, int64_t pos0, float base,
+                             const float* factors, int inverse, void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks, before any CUDA call
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size");
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (inverse != 0 && inverse != 1) return fail(VATTN_ERR_INVALID_ARG, "inverse must be 0 or 1");
+  vattn_status st = check_rope(head_dim, n_patches, rope_dims, pos0, base, factors);
+  if (st != VATTN_OK) return st;
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  const int half = static_cast<int>(rope_dims / 2);
+  if (bh == 0 || n_patches == 0 || half == 0) return VATTN_OK;  // nothing turns
+  if (!x) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT64_MAX / n_patches || bh * n_patches > INT64_MAX / head_dim)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor size overflows");
+  if (reinterpret_cast<uintptr_t>(x) & 3u)
+    return fail(VATTN_ERR_MISALIGNED, "x must be 4-byte aligned");
+
+  // ---- device side: angle table (stream-ordered workspace), then the turn
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaMemPool_t pool = nullptr;
+  if ((st = pool_for(device, &pool)) != VATTN_OK) return st;
+  void* tab = nullptr;
+  e = cudaMallocFromPoolAsync(&tab, static_cast<size_t>(n_patches) * half * sizeof(float2), pool,
+                              stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  const int N = static_cast<int>(n_patches);
+  auto grid_for = [](long long items) {
+    const long long blocks = (items + 255) / 256;
+    return static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
+  };
+  vattn::vattn_rope_table_kernel<<<grid_for(static_cast<long long>(N) * half), 256, 0, stream>>>(
+      static_cast<float2*>(tab), N, half, static_cast<int>(rope_dims), pos0, base, factors);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    st = cuda_fail(e, "RoPE table kernel launch");
+  } else {
+    const long long rows = bh * n_patches;
+    const bool by4 = (half % 4 == 0) && (head_dim % 4 == 0) &&
+                     (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+    if (by4)
+      vattn::vattn_rope_apply4_kernel<<<grid_for(rows * (half / 4)), 256, 0, stream>>>(
+          x, rows, N, static_cast<int>(head_dim), half, static_cast<const float2*>(tab), inverse);
+    else
+      vattn::vattn_rope_apply_kernel<<<grid_for(rows * half), 256, 0, stream>>>(
+          x, rows, N, static_cast<int>(head_dim), half, static_cast<const float2*>(tab), inverse);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) st = cuda_fail(e, "RoPE kernel launch");
+  }
+  e = cudaFreeAsync(tab, stream);
+  if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
+  return st;
+}
+
+vattn_status vattn_forward_rope(const float* q, const float* k, const float* v, float* out,
+                                int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, int64_t rope_dims, int64_t pos0, float base,
+                                const float* factors, void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks (those of vattn_forward and of the rotation)
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
+                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (head_dim > VATTN_MAX_HEAD_DIM)
+    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  vattn_status st = check_rope(head_dim, n_patches, rope_dims, pos0, base, factors);
+  if (st != VATTN_OK) return st;
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
+  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
+  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+
+  const int D = static_cast<int>(head_dim);
+  const int N = static_cast<int>(n_patches);
+  const int d_pad = (D + 15) & ~15;
+  const int half = static_cast<int>(rope_dims / 2);
+  const int nkb = d_pad <= 64 ? 1 : 2;
+  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+  vattn::Params p{};
+  p.out = out;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = d_pad;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+
+  // ---- device side: workspace = f16 copies of q, k, v + the angle table
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int64_t rows = bh * N;
+  const size_t region = (static_cast<size_t>(rows) * d_pad * 2 + 255) & ~static_cast<size_t>(255);
+  const size_t tab_bytes = static_cast<size_t>(N) * (half > 0 ? half : 1) * sizeof(float2);
+  cudaMemPool_t pool = nullptr;
+  if ((st = pool_for(device, &pool)) != VATTN_OK) return st;
+  void* ws = nullptr;
+  e = cudaMallocFromPoolAsync(&ws, 3 * region + tab_bytes, pool, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  __half* q16 = static_cast<__half*>(ws);
+  __half* k16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + region);
+  __half* v16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + 2 * region);
+  float2* tab = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + 3 * region);
+
+  CUtensorMap tq, tk, tv;
+  if ((st = make_tmap16(&tq, q16, bh, N, d_pad)) == VATTN_OK &&
+      (st = make_tmap16(&tk, k16, bh, N, d_pad)) == VATTN_OK &&
+      (st = make_tmap16(&tv, v16, bh, N, d_pad)) == VATTN_OK) {
+    auto grid_for = [](long long items) {
+      const long long blocks = (items + 255) / 256;
+      return static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
+    };
+    if (half > 0) {
+      vattn::vattn_rope_table_kernel<<<grid_for(static_cast<long long>(N) * half), 256, 0, stream>>>(
+          tab, N, half, static_cast<int>(rope_dims), pos0, base, factors);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) st = cuda_fail(e, "RoPE table kernel launch");
+    }
+    const int vec = (D % 8 == 0) &&
+                    ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                      reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+    if (st == VATTN_OK) {
+      vattn::vattn_stage_rope_kernel<<<grid_for(3LL * rows * (d_pad / 8)), 256, 0, stream>>>(
+          vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, rows, N, D,
+          d_pad, half, tab, vec);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) st = cuda_fail(e, "staging kernel launch");
+    }
+    if (st == VATTN_OK) {
+      const unsigned g = static_cast<unsigned>(grid);
+      if (nkb == 1 && nq == 2)
+        st = launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
+      else if (nkb == 1)
+        st = launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
+      else
+        st = launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+    }
+  }
+  e = cudaFreeAsync(ws, stream);
+  if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
+  return st;
 }
 
 vattn_status vattn_device_status(uint32_t* code) {
