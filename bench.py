@@ -447,12 +447,26 @@ def run_vattn(args, workload):
         torch.cuda.synchronize(dev)
         rms = a.elapsed_time(b2) / reps
         rbytes = 3 * B * H * N * (D // 2 * 2) * 4 * 2
+        x16 = [t.half() for t in (qd, kd, vd)]
+        o16 = torch.empty_like(x16[0])
+        for _ in range(10):
+            vef.forward_f16io(*x16, out=o16)
+        a.record(stream)
+        for _ in range(reps):
+            vef.forward_f16io(*x16, out=o16)
+        b2.record(stream)
+        torch.cuda.synchronize(dev)
+        f16io_ms = a.elapsed_time(b2) / reps
+        del x16, o16
         if vef.device_status() != 0:
             raise RuntimeError("kernel reported a wait timeout")
         variants = {
             "rope_fused_call": {"ms": round(fms, 5), "tflops": round(flops / fms / 1e9, 2),
                                 "vs_plain_call": round(fms / ms_per_step, 4),
                                 "what": "vattn_forward_rope, rope_dims = head_dim, pos0 0, base 1e4"},
+            "f16io_kernel": {"ms": round(f16io_ms, 5), "tflops": round(flops / f16io_ms / 1e9, 2),
+                             "frac_of_peak": round(flops / f16io_ms / 1e9 / peak_tf, 4),
+                             "what": "vattn_forward_f16io: the attention kernel alone, f16 in and out"},
             "rope_inplace": {"ms": round(rms, 5), "bytes": rbytes,
                              "achieved_gbs": round(rbytes / (rms * 1e-3) / 1e9, 1),
                              "frac_of_hbm": round(rbytes / (rms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4),

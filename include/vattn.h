@@ -101,6 +101,23 @@ vattn_status vattn_forward_f16(const uint16_t* q, const uint16_t* k, const uint1
                                int64_t head_dim, void* stream);
 
 /*
+ * vattn_forward_f16io -- vattn_forward_f16 with an f16 output: each output
+ * element is the f32 value vattn_forward_f16 would store, rounded to f16
+ * (round to nearest even).  Halves the output bytes for callers that keep
+ * activations in f16.
+ *
+ * q, k, v: as for vattn_forward_f16 (f16, head_dim % 8 == 0, 16-byte
+ *   aligned).  out: DEVICE pointer to IEEE binary16 [batch, n_heads,
+ *   n_patches, head_dim], 2-byte aligned (16-byte aligned lets the kernel
+ *   write it with bulk tensor stores), not overlapping q, k or v.
+ * Asynchronous, no allocation, one kernel launch; errors as for
+ * vattn_forward_f16.
+ */
+vattn_status vattn_forward_f16io(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 uint16_t* out, int64_t batch, int64_t n_heads,
+                                 int64_t n_patches, int64_t head_dim, void* stream);
+
+/*
  * vattn_rope_neox -- NeoX rotary position embedding, in place.
  *
  * The rotation of the WGSL kernel "rope_neox_backward.wgsl" (rullama 0.2.0):

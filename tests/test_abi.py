@@ -18,7 +18,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = _lib.exported_symbols()
-    assert set(names) == {"vattn_forward", "vattn_forward_f16", "vattn_forward_noalloc",
+    assert set(names) == {"vattn_forward", "vattn_forward_f16", "vattn_forward_f16io",
+                          "vattn_forward_noalloc",
                           "vattn_rope_neox", "vattn_forward_rope",
                           "vattn_device_status", "vattn_status_string",
                           "vattn_last_error_string", "vattn_version"}
@@ -186,3 +187,24 @@ def test_rope_no_ops_need_no_pointer(lib, args):
 def test_forward_rope_host_side_argument_errors(lib, args, status):
     assert _lib.forward_rope_status(*args, 0) == status
     assert lib.vattn_last_error_string().decode() != ""
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 12), 2),      # head_dim % 8 != 0
+    ((FAKE + 8, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 8), 3),   # f16 inputs need 16 bytes
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30 + 1, 1, 2, 3, 8), 3),   # f16 out needs 2 bytes
+    # f16 out (same bytes as an input) overlaps v: v starts 64 bytes after out
+    ((FAKE + 2 ** 20, FAKE + 2 ** 21, FAKE + 64, FAKE, 1, 2, 3, 8), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 3, 136), 2),
+])
+def test_f16io_entry_host_side_argument_errors(lib, args, status):
+    assert _lib.forward_f16io_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""
+
+
+def test_f16io_entry_out_may_sit_right_after_an_input(lib):
+    """f16 out of 1 x 2 x 3 x 8 = 96 bytes starting where v's 96 bytes end is
+    no overlap; the call gets past the host checks (no GPU: CUDA error 4)."""
+    status = _lib.forward_f16io_status(FAKE, FAKE + 2 ** 20, FAKE + 2 ** 21,
+                                       FAKE + 2 ** 21 + 96, 1, 2, 3, 8, 0)
+    assert status in (0, 4)

@@ -116,3 +116,53 @@ def test_f16_entry_on_a_side_stream(torch_dev):
     assert vef.device_status() == 0
     ref = run_f16(torch_dev, to_f16(q), to_f16(k), to_f16(v))
     assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def run_f16io(torch_dev, q16, k16, v16, out_offset=0):
+    """vattn_forward_f16io; out_offset (in f16 elements) shifts the output
+    inside a larger buffer to exercise an output that is only 2-byte aligned."""
+    torch, dev = torch_dev
+    qd, kd, vd = (torch.from_numpy(x).to(dev) for x in (q16, k16, v16))
+    buf = torch.full((qd.numel() + out_offset,), float("nan"), dtype=torch.float16, device=dev)
+    out = buf[out_offset:].view(qd.shape)
+    if out_offset:
+        B, H, N, D = qd.shape
+        status = vef._lib.forward_f16io_status(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(),
+                                               out.data_ptr(), B, H, N, D,
+                                               torch.cuda.current_stream(dev).cuda_stream)
+        assert status == 0
+    else:
+        vef.forward_f16io(qd, kd, vd, out=out)
+    torch.cuda.synchronize(dev)
+    assert vef.device_status() == 0
+    return out.cpu().numpy()
+
+
+F16IO_SHAPES = [(1, 2, 64, 32), (2, 3, 200, 40), (1, 16, 256, 64), (2, 2, 130, 72),
+                (1, 2, 300, 128), (3, 1, 129, 8), (1, 4, 257, 64)]
+
+
+@pytest.mark.parametrize("shape", F16IO_SHAPES)
+@pytest.mark.parametrize("out_offset", [0, 1])
+def test_f16io_is_the_f16_entry_rounded_to_f16(torch_dev, shape, out_offset):
+    """Bit for bit: the f16 output is the f32 output of vattn_forward_f16
+    rounded to nearest even (numpy's float16 cast), for the bulk-store
+    epilogue (head_dim <= 64, 16-byte aligned out) and the per-thread one."""
+    q, k, v = make_inputs(*shape, seed=888 + sum(shape))
+    q16, k16, v16 = to_f16(q), to_f16(k), to_f16(v)
+    got = run_f16io(torch_dev, q16, k16, v16, out_offset)
+    ref = run_f16(torch_dev, q16, k16, v16).astype(np.float16)
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), f"{shape}: differs"
+
+
+def test_f16io_on_the_largest_workload_sampled(torch_dev):
+    q, k, v = workload_inputs(5)
+    q16, k16, v16 = to_f16(q), to_f16(k), to_f16(v)
+    got = run_f16io(torch_dev, q16, k16, v16).astype(np.float32)
+    b, h, n, d = q.shape
+    rows = np.random.default_rng(55).integers(0, b * h * n, 192)
+    ref = oracle.rows(*(x.astype(np.float32) for x in (q16, k16, v16)), rows)
+    diff = got.reshape(-1, d)[rows].astype(np.float64) - ref
+    # f16 output rounding (2^-11 relative) on top of the kernel-arithmetic bound
+    bound = (2.0 ** -10 + n * 2.0 ** -24) * float(np.abs(v16.astype(np.float32)).max()) + 1e-5
+    assert float(np.abs(diff).max()) <= bound

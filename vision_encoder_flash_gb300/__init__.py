@@ -10,10 +10,11 @@ missing or no GPU is present the calls raise.
 from __future__ import annotations
 
 from ._lib import (VattnError, _check, device_status, exported_symbols, forward_f16_raw,
+                   forward_f16io_status,
                    forward_noalloc_raw, forward_raw, forward_rope_status, lib_path,
                    load_library, rope_neox_status, status_string, version)
 
-__all__ = ["forward", "forward_f16", "forward_rope", "rope_neox", "forward_raw",
+__all__ = ["forward", "forward_f16", "forward_f16io", "forward_rope", "rope_neox", "forward_raw",
            "forward_f16_raw", "forward_noalloc_raw",
            "device_status", "VattnError", "load_library",
            "lib_path", "exported_symbols", "status_string", "version"]
@@ -96,6 +97,31 @@ def forward_f16(q, k, v, out=None, stream=None):
     B, H, N, D = q.shape
     forward_f16_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D,
                     s.cuda_stream)
+    return out
+
+
+def forward_f16io(q, k, v, out=None, stream=None):
+    """out (f16) = softmax(q k^T) v for CUDA float16 tensors ``[B, H, N, D]``
+    (``D`` a multiple of 8): the output of ``forward_f16`` rounded to f16.
+    Runs on ``stream`` (default: the current torch stream); no synchronisation."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float16:
+            raise TypeError(f"{name} must be a float16 torch.Tensor")
+        if t.dim() != 4 or t.device.type != "cuda" or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA [batch, n_heads, n_patches, head_dim]")
+    if not (q.shape == k.shape == v.shape) or not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must have one shape and one device")
+    if out is None:
+        out = torch.empty_like(q)
+    if out.shape != q.shape or out.dtype != torch.float16 or out.device != q.device \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float16 tensor of q's shape and device")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    B, H, N, D = q.shape
+    _check(forward_f16io_status(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N,
+                                D, s.cuda_stream))
     return out
 
 

@@ -43,6 +43,8 @@ def load_library():
     lib.vattn_rope_neox.restype = ctypes.c_int
     lib.vattn_forward_rope.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp]
     lib.vattn_forward_rope.restype = ctypes.c_int
+    lib.vattn_forward_f16io.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.vattn_forward_f16io.restype = ctypes.c_int
     lib.vattn_forward_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_f16.restype = ctypes.c_int
     lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
@@ -91,6 +93,13 @@ def forward_f16_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, 
     """Like forward_f16_raw but returns the status code instead of raising."""
     return int(load_library().vattn_forward_f16(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                                 n_patches, head_dim, stream))
+
+
+def forward_f16io_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,
+                         stream=0) -> int:
+    """vattn_forward_f16io with device addresses (f16 in, f16 out); returns the status."""
+    return int(load_library().vattn_forward_f16io(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                                  n_patches, head_dim, stream))
 
 
 def rope_neox_status(x_ptr, batch, n_heads, n_patches, head_dim, rope_dims, pos0, base,

@@ -73,7 +73,8 @@ constexpr uint32_t kStatusTimeout = 0x100u;
 __device__ uint32_t g_vattn_status;
 
 struct Params {
-  float* out;
+  float* out;       // f32 output (kOut16 == false)
+  uint16_t* out16;  // f16 output (kOut16 == true): IEEE binary16, round to nearest even
   int n_patches;  // N
   int head_dim;   // D
   int d_pad;      // D rounded up to 16
@@ -188,7 +189,9 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
 // handles tiles b, b + gridDim.x, ... (gridDim.x <= n_tiles).
 // tm_q / tm_k / tm_v: f16 [B*H, N, d_pad] with boxes of {64 columns, 128 rows},
 // 128-byte swizzle (columns past d_pad and rows past N read as zero).
-template <int NQ, int NKB>
+// kOut16: the output is rounded to f16 (round to nearest even) instead of
+// written in f32.
+template <int NQ, int NKB, bool kOut16 = false>
 __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
     vattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -515,14 +518,30 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
           __syncwarp();
           ptx::tmem_wait_ld_dep16(y);
           const uint32_t buf = epi + static_cast<uint32_t>(c & 1) * 2048u;
-          const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 64u;
+          if constexpr (kOut16) {
+            // 32 bytes per row, 32-byte swizzle (16-byte unit k at k ^ ((row >> 2) & 1))
+            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 32u;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(k) ^ ((lane >> 1) & 3u)) << 4),
-                              __uint_as_float(y[4 * k + 0]) * inv_l,
-                              __uint_as_float(y[4 * k + 1]) * inv_l,
-                              __uint_as_float(y[4 * k + 2]) * inv_l,
-                              __uint_as_float(y[4 * k + 3]) * inv_l);
+            for (int k = 0; k < 2; ++k) {
+              uint32_t h[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                h[e] = ptx::pack_half2(__uint_as_float(y[8 * k + 2 * e]) * inv_l,
+                                       __uint_as_float(y[8 * k + 2 * e + 1]) * inv_l);
+              ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(k) ^ ((lane >> 2) & 1u)) << 4),
+                                __uint_as_float(h[0]), __uint_as_float(h[1]),
+                                __uint_as_float(h[2]), __uint_as_float(h[3]));
+            }
+          } else {
+            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(k) ^ ((lane >> 1) & 3u)) << 4),
+                                __uint_as_float(y[4 * k + 0]) * inv_l,
+                                __uint_as_float(y[4 * k + 1]) * inv_l,
+                                __uint_as_float(y[4 * k + 2]) * inv_l,
+                                __uint_as_float(y[4 * k + 3]) * inv_l);
+          }
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -535,6 +554,26 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
       }
       const int row = tile_row0(i) + t * kBM + quarter * 32 + lane;
       const int D = p.head_dim;
+      if constexpr (kOut16) {
+        uint16_t* orow16 = p.out16 + (static_cast<size_t>(tile_bh(i)) * N + row) * D;
+        for (int c = 0; c < (p.d_pad >> 4); ++c) {
+          uint32_t y[16];
+          ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
+          ptx::tmem_wait_ld_dep16(y);
+          if (row < N) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int d = c * 16 + e;
+              const uint32_t h = ptx::pack_half2(__uint_as_float(y[e]) * inv_l,
+                                                 __uint_as_float(y[e + 1]) * inv_l);
+              if (d < D) orow16[d] = static_cast<uint16_t>(h & 0xFFFFu);
+              if (d + 1 < D) orow16[d + 1] = static_cast<uint16_t>(h >> 16);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        continue;
+      }
       float* orow = p.out + (static_cast<size_t>(tile_bh(i)) * N + row) * D;
       for (int c = 0; c < (p.d_pad >> 4); ++c) {
         uint32_t y[16];

@@ -86,11 +86,12 @@ vattn_status make_tmap16(CUtensorMap* tm, const __half* ptr, int64_t bh, int64_t
   return VATTN_OK;
 }
 
-// 3-D view {head_dim, n_patches, batch*n_heads} of the f32 output for the
-// kernel's TMA stores: box = 32 rows x 16 columns (64 bytes), 64-byte swizzle
-// (the layout the kernel writes to its staging buffers).  Needs head_dim % 4
-// == 0 and a 16-byte aligned base.
-vattn_status make_tmap_out(CUtensorMap* tm, float* out, int64_t bh, int64_t n, int d) {
+// 3-D view {head_dim, n_patches, batch*n_heads} of the output for the
+// kernel's TMA stores: box = 32 rows x 16 columns, f32 (64 bytes, 64-byte
+// swizzle) or f16 (32 bytes, 32-byte swizzle): the layouts the kernel writes
+// to its staging buffers.  Needs rows of whole 16-byte units (head_dim % 4 ==
+// 0 for f32, % 8 == 0 for f16) and a 16-byte aligned base.
+vattn_status make_tmap_out(CUtensorMap* tm, void* out, int64_t bh, int64_t n, int d, bool f16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     if (g_encode_err != cudaSuccess) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
@@ -98,12 +99,14 @@ vattn_status make_tmap_out(CUtensorMap* tm, float* out, int64_t bh, int64_t n, i
   }
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
                               static_cast<cuuint64_t>(bh)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4u,
-                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(d) * 4u};
+  const cuuint64_t esize = f16 ? 2u : 4u;
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esize,
+                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(d) * esize};
   const cuuint32_t box[3] = {16u, 32u, 1u};
   const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
-  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box,
-                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+  const CUresult r = enc(tm, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         3, out, dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         f16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled (out) failed with CUresult %d", static_cast<int>(r));
@@ -157,12 +160,12 @@ vattn_status sm_count(int device, int* out) {
 
 // The attention kernel is persistent: one block per multiprocessor (at most
 // one per tile), each looping over the tiles blockIdx.x + k * gridDim.x.
-template <int NQ, int NKB>
+template <int NQ, int NKB, bool kOut16 = false>
 vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               vattn::Params p, unsigned n_tiles, cudaStream_t stream,
                               int device) {
   using P = vattn::Plan<NQ, NKB>;
-  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB>;
+  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kOut16>;
   static std::atomic<uint8_t> configured[kMaxDevices];
   if (!configured[device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -180,8 +183,9 @@ vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, cons
   std::memset(&to, 0, sizeof(to));
   p.tma_out = 0;
   if (NKB == 1 && p.vec_out) {
-    const vattn_status so = make_tmap_out(&to, p.out, static_cast<int64_t>(p.n_tiles / p.n_qblocks),
-                                          p.n_patches, p.head_dim);
+    void* out_base = kOut16 ? static_cast<void*>(p.out16) : static_cast<void*>(p.out);
+    const vattn_status so = make_tmap_out(&to, out_base, static_cast<int64_t>(p.n_tiles / p.n_qblocks),
+                                          p.n_patches, p.head_dim, kOut16);
     if (so != VATTN_OK) return so;
     p.tma_out = 1;
   }
@@ -217,6 +221,82 @@ bool overlaps(const void* a, const void* b, uint64_t bytes) {
 bool overlaps2(const void* a, uint64_t a_bytes, const void* b, uint64_t b_bytes) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + b_bytes && y < x + a_bytes;
+}
+
+// The attention kernel alone on f16 inputs; out is f32 (kOut16 == false) or
+// f16 (kOut16 == true).
+template <bool kOut16>
+vattn_status forward_f16_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, void* out,
+                              int64_t batch, int64_t n_heads, int64_t n_patches,
+                              int64_t head_dim, void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks, before any CUDA call
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
+                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (head_dim > VATTN_MAX_HEAD_DIM)
+    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  if (head_dim % 8 != 0)
+    return fail(VATTN_ERR_UNSUPPORTED,
+                "f16 inputs need head_dim %% 8 == 0 (16-byte rows), got %lld: use vattn_forward",
+                (long long)head_dim);
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t in_bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 2u;
+  const uint64_t out_bytes = kOut16 ? in_bytes : 2u * in_bytes;
+  if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+        reinterpret_cast<uintptr_t>(v)) & 15u) != 0)
+    return fail(VATTN_ERR_MISALIGNED, "f16 q, k, v must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(out) & (kOut16 ? 1u : 3u))
+    return fail(VATTN_ERR_MISALIGNED, kOut16 ? "out must be 2-byte aligned" : "out must be 4-byte aligned");
+  if (overlaps2(out, out_bytes, q, in_bytes) || overlaps2(out, out_bytes, k, in_bytes) ||
+      overlaps2(out, out_bytes, v, in_bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+
+  const int D = static_cast<int>(head_dim);
+  const int N = static_cast<int>(n_patches);
+  const int d_pad = (D + 15) & ~15;
+  const int nkb = d_pad <= 64 ? 1 : 2;
+  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+
+  vattn::Params p{};
+  p.out = kOut16 ? nullptr : static_cast<float*>(out);
+  p.out16 = kOut16 ? static_cast<uint16_t*>(out) : nullptr;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = d_pad;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (D % (kOut16 ? 8 : 4) == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+
+  // ---- device side: the tensor maps read the caller's rows of D elements;
+  // columns D..d_pad-1 read as zero
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
+  CUtensorMap tq, tk, tv;
+  vattn_status st;
+  if ((st = make_tmap16(&tq, reinterpret_cast<const __half*>(q), bh, N, D)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tk, reinterpret_cast<const __half*>(k), bh, N, D)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tv, reinterpret_cast<const __half*>(v), bh, N, D)) != VATTN_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const unsigned g = static_cast<unsigned>(grid);
+  if (nkb == 1 && nq == 2) return launch_attention<2, 1, kOut16>(tq, tk, tv, p, g, stream, device);
+  if (nkb == 1) return launch_attention<1, 1, kOut16>(tq, tk, tv, p, g, stream, device);
+  return launch_attention<1, 2, kOut16>(tq, tk, tv, p, g, stream, device);
 }
 
 }  // namespace
@@ -323,73 +403,13 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
 vattn_status vattn_forward_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                float* out, int64_t batch, int64_t n_heads, int64_t n_patches,
                                int64_t head_dim, void* stream_ptr) {
-  g_last_error[0] = '\0';
-  // ---- host-side checks, before any CUDA call
-  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
-    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
-                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
-  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
-  if (head_dim > VATTN_MAX_HEAD_DIM)
-    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
-  if (head_dim % 8 != 0)
-    return fail(VATTN_ERR_UNSUPPORTED,
-                "f16 inputs need head_dim %% 8 == 0 (16-byte rows), got %lld: use vattn_forward",
-                (long long)head_dim);
-  if (batch != 0 && n_heads > INT64_MAX / batch)
-    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
-  const int64_t bh = batch * n_heads;
-  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
-  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
-  if (n_patches > INT32_MAX || bh > INT32_MAX)
-    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
-  if (n_patches > INT64_MAX / head_dim / bh / 4)
-    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
-  const uint64_t in_bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 2u;
-  const uint64_t out_bytes = 2u * in_bytes;
-  if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-        reinterpret_cast<uintptr_t>(v)) & 15u) != 0)
-    return fail(VATTN_ERR_MISALIGNED, "f16 q, k, v must be 16-byte aligned");
-  if (reinterpret_cast<uintptr_t>(out) & 3u)
-    return fail(VATTN_ERR_MISALIGNED, "out must be 4-byte aligned");
-  if (overlaps2(out, out_bytes, q, in_bytes) || overlaps2(out, out_bytes, k, in_bytes) ||
-      overlaps2(out, out_bytes, v, in_bytes))
-    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+  return forward_f16_impl<false>(q, k, v, out, batch, n_heads, n_patches, head_dim, stream_ptr);
+}
 
-  const int D = static_cast<int>(head_dim);
-  const int N = static_cast<int>(n_patches);
-  const int d_pad = (D + 15) & ~15;
-  const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
-  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
-  const int64_t grid = bh * n_qblocks;
-  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
-
-  vattn::Params p{};
-  p.out = out;
-  p.n_patches = N;
-  p.head_dim = D;
-  p.d_pad = d_pad;
-  p.n_qblocks = static_cast<int>(n_qblocks);
-  p.n_tiles = static_cast<int>(grid);
-  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
-  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
-
-  // ---- device side: the tensor maps read the caller's rows of D elements;
-  // columns D..d_pad-1 read as zero
-  int device = 0;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
-  CUtensorMap tq, tk, tv;
-  vattn_status st;
-  if ((st = make_tmap16(&tq, reinterpret_cast<const __half*>(q), bh, N, D)) != VATTN_OK) return st;
-  if ((st = make_tmap16(&tk, reinterpret_cast<const __half*>(k), bh, N, D)) != VATTN_OK) return st;
-  if ((st = make_tmap16(&tv, reinterpret_cast<const __half*>(v), bh, N, D)) != VATTN_OK) return st;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const unsigned g = static_cast<unsigned>(grid);
-  if (nkb == 1 && nq == 2) return launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
-  if (nkb == 1) return launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
-  return launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+vattn_status vattn_forward_f16io(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 uint16_t* out, int64_t batch, int64_t n_heads,
+                                 int64_t n_patches, int64_t head_dim, void* stream_ptr) {
+  return forward_f16_impl<true>(q, k, v, out, batch, n_heads, n_patches, head_dim, stream_ptr);
 }
 
 vattn_status vattn_rope_neox(float* x, int64_t batch, int64_t n_heads, int64_t n_patches,
