@@ -458,9 +458,22 @@ def run_vattn(args, workload):
         torch.cuda.synchronize(dev)
         f16io_ms = a.elapsed_time(b2) / reps
         del x16, o16
+        for _ in range(5):
+            vef.forward_accurate(qd, kd, vd, out=out)
+        a.record(stream)
+        for _ in range(reps // 4):
+            vef.forward_accurate(qd, kd, vd, out=out)
+        b2.record(stream)
+        torch.cuda.synchronize(dev)
+        acc_ms = a.elapsed_time(b2) / (reps // 4)
         if vef.device_status() != 0:
             raise RuntimeError("kernel reported a wait timeout")
         variants = {
+            "accurate_call": {"ms": round(acc_ms, 5), "tflops": round(flops / acc_ms / 1e9, 2),
+                              "tensor_tflops": round(3 * flops / acc_ms / 1e9, 2),
+                              "vs_plain_call": round(acc_ms / ms_per_step, 4),
+                              "what": "vattn_forward_accurate (split-f16, three products per "
+                                      "matrix product; tflops counts the algorithmic flops once)"},
             "rope_fused_call": {"ms": round(fms, 5), "tflops": round(flops / fms / 1e9, 2),
                                 "vs_plain_call": round(fms / ms_per_step, 4),
                                 "what": "vattn_forward_rope, rope_dims = head_dim, pos0 0, base 1e4"},

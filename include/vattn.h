@@ -161,6 +161,31 @@ vattn_status vattn_forward_rope(const float* q, const float* k, const float* v, 
                                 const float* factors, void* stream);
 
 /*
+ * vattn_forward_accurate -- the attention of vattn_forward without the f16
+ * rounding of the operands, to about f32 accuracy.
+ *
+ * The shader's header comment names a sibling variant, "sub", that keeps
+ * q, k, v and the tile scores in f32 workgroup storage instead of f16; this
+ * call is its counterpart.  It keeps the tensor cores by splitting every
+ * operand in two f16 terms, x = hi + lo with hi = f16(x) and
+ * lo = f16(x - hi) (round to nearest even), which represents x to about
+ * 2^-22 relative, and takes three products for each of the two matrix
+ * products:  S = Qh Kh^T + Qh Kl^T + Ql Kh^T  and, with the softmax weights
+ * split the same way,  O += Ph Vh + Ph Vl + Pl Vh  (the dropped lo x lo
+ * terms are below 2^-22 relative), all accumulated in f32.  Statistics,
+ * accumulator and output are f32 as in vattn_forward.  It costs about three
+ * times the tensor work of vattn_forward and twice its staged bytes.
+ *
+ * Arguments, layout, ownership and error codes: those of vattn_forward.
+ * Workspace: six f16 tensors (hi and lo of q, k, v), 2 x vattn_forward's,
+ * from the same per-device pool, stream-ordered.  Asynchronous; two kernel
+ * launches; empty problems are a no-op.
+ */
+vattn_status vattn_forward_accurate(const float* q, const float* k, const float* v, float* out,
+                                    int64_t batch, int64_t n_heads, int64_t n_patches,
+                                    int64_t head_dim, void* stream);
+
+/*
  * Size of the fixed staging scratch of vattn_forward_noalloc: 32 MiB, enough
  * for batch*n_heads*n_patches*round_up(head_dim, 16) <= 5,592,320 (for
  * example 16 heads x 4,100 patches at head_dim 72, or 64 heads x 1,024

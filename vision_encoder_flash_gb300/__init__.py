@@ -9,12 +9,12 @@ missing or no GPU is present the calls raise.
 """
 from __future__ import annotations
 
-from ._lib import (VattnError, _check, device_status, exported_symbols, forward_f16_raw,
-                   forward_f16io_status,
+from ._lib import (VattnError, _check, device_status, exported_symbols, forward_accurate_status,
+                   forward_f16_raw, forward_f16io_status,
                    forward_noalloc_raw, forward_raw, forward_rope_status, lib_path,
                    load_library, rope_neox_status, status_string, version)
 
-__all__ = ["forward", "forward_f16", "forward_f16io", "forward_rope", "rope_neox", "forward_raw",
+__all__ = ["forward", "forward_accurate", "forward_f16", "forward_f16io", "forward_rope", "rope_neox", "forward_raw",
            "forward_f16_raw", "forward_noalloc_raw",
            "device_status", "VattnError", "load_library",
            "lib_path", "exported_symbols", "status_string", "version"]
@@ -185,6 +185,31 @@ def forward_rope(q, k, v, rope_dims, pos0=0, base=10000.0, factors=None, out=Non
     _check(forward_rope_status(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N,
                                D, rope_dims, pos0, float(base),
                                _factors_ptr(factors, rope_dims, q.device), s.cuda_stream))
+    return out
+
+
+def forward_accurate(q, k, v, out=None, stream=None):
+    """out = softmax(q k^T) v for CUDA f32 tensors ``[B, H, N, D]`` to about
+    f32 accuracy: every operand is split into two f16 terms and each matrix
+    product takes three tensor-core products.  Returns ``out`` without
+    synchronising."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_f32(name, t)
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [batch, n_heads, n_patches, head_dim]")
+    if not (q.shape == k.shape == v.shape) or not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must have one shape and one device")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_f32("out", out)
+    if out.shape != q.shape or out.device != q.device:
+        raise ValueError("out must match q in shape and device")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    B, H, N, D = q.shape
+    _check(forward_accurate_status(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                                   N, D, s.cuda_stream))
     return out
 
 

@@ -47,6 +47,8 @@ def load_library():
     lib.vattn_forward_f16io.restype = ctypes.c_int
     lib.vattn_forward_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_f16.restype = ctypes.c_int
+    lib.vattn_forward_accurate.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.vattn_forward_accurate.restype = ctypes.c_int
     lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_noalloc.restype = ctypes.c_int
     lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -116,6 +118,14 @@ def forward_rope_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches,
     return int(load_library().vattn_forward_rope(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                                  n_patches, head_dim, rope_dims, pos0, base,
                                                  factors_ptr, stream))
+
+
+def forward_accurate_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,
+                            stream=0) -> int:
+    """vattn_forward_accurate (split-f16, about f32 accuracy) with device
+    addresses; returns the status code."""
+    return int(load_library().vattn_forward_accurate(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                                     n_patches, head_dim, stream))
 
 
 def forward_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int,

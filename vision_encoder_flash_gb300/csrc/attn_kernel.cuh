@@ -87,18 +87,23 @@ struct Params {
 
 // Shared-memory plan for NQ query tiles and NKB 64-column blocks of d_pad.
 // f16 tiles: NKB blocks of [128 rows x 128 bytes], 128-byte swizzle.
-template <int NQ, int NKB>
+// kAcc (accurate mode, one query tile): every Q, K and V tile comes as an
+// f16 pair (hi, lo), the lo part right after the hi part.
+template <int NQ, int NKB, bool kAcc = false>
 struct Plan {
   static constexpr int kThreads = 128 * (1 + NQ);  // control warpgroup + softmax
   static constexpr int kTileF16 = NKB * kBoxBytes;
-  static constexpr int kStages = NKB == 1 ? 5 : 3;  // K and V stages
+  static constexpr int kParts = kAcc ? 2 : 1;      // f16 terms per operand
+  static constexpr int kPartBytes = kTileF16;      // offset of lo after hi
+  static constexpr int kStageStride = kParts * kTileF16;
+  static constexpr int kStages = kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : 3);  // K and V stages
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + NQ * kTileF16;
-  static constexpr int kOffV = kOffK + kStages * kTileF16;
+  static constexpr int kOffK = kOffQ + NQ * kStageStride;
+  static constexpr int kOffV = kOffK + kStages * kStageStride;
   // output staging for the TMA-store epilogue (head_dim <= 64 only): two
   // 2 KB buffers (32 rows x 16 f32, 64-byte swizzle) per softmax warp
-  static constexpr int kEpiBytes = NKB == 1 ? 4 * NQ * 4096 : 0;
-  static constexpr int kOffEpi = kOffV + kStages * kTileF16;
+  static constexpr int kEpiBytes = (NKB == 1 && !kAcc) ? 4 * NQ * 4096 : 0;
+  static constexpr int kOffEpi = kOffV + kStages * kStageStride;
   static constexpr int kOffBar = kOffEpi + kEpiBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
@@ -107,14 +112,16 @@ struct Plan {
   static constexpr bool kSplitRegs = NQ == 2;
   static constexpr uint32_t kRegsSoftmax = 224;
   static constexpr uint32_t kRegsOther = 56;
-  // TMEM columns
+  // TMEM columns (kAcc: P hi at 256, P lo at 320, O at 384)
   static constexpr uint32_t kColP = 256;
-  static constexpr uint32_t kColO = NQ == 2 ? 384 : 320;
+  static constexpr uint32_t kColPlo = 320;
+  static constexpr uint32_t kColO = (NQ == 2 || kAcc) ? 384 : 320;
   static constexpr uint32_t kColStride = 64;  // between the tiles' P (and O) blocks
   static_assert(!kSplitRegs || kRegsOther + NQ * kRegsSoftmax <= (1 + NQ) * 168,
                 "register split too large");
   static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
   static_assert(NQ == 1 || NKB == 1, "two query tiles need head_dim <= 64");
+  static_assert(!kAcc || NQ == 1, "the accurate mode takes one query tile");
 };
 
 // mbarrier indices inside the barrier block (kStages <= 5).
@@ -191,13 +198,21 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
 // 128-byte swizzle (columns past d_pad and rows past N read as zero).
 // kOut16: the output is rounded to f16 (round to nearest even) instead of
 // written in f32.
-template <int NQ, int NKB, bool kOut16 = false>
-__global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
+// kAcc: accurate mode.  q, k, v arrive as f16 pairs (hi, lo; the lo tensor
+// maps are tm_ql, tm_kl, tm_vl), the softmax weights are split the same way
+// into P hi and P lo, and each product takes three MMAs:
+//   S = Qh Kh^T + Qh Kl^T + Ql Kh^T,   O += Ph Vh + Ph Vl + Pl Vh
+// (the lo x lo terms are below 2^-22 relative).
+template <int NQ, int NKB, bool kOut16 = false, bool kAcc = false>
+__global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
     vattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_o, const Params p) {
-  using P = Plan<NQ, NKB>;
+                     const __grid_constant__ CUtensorMap tm_o,
+                     const __grid_constant__ CUtensorMap tm_ql,
+                     const __grid_constant__ CUtensorMap tm_kl,
+                     const __grid_constant__ CUtensorMap tm_vl, const Params p) {
+  using P = Plan<NQ, NKB, kAcc>;
   constexpr int S = P::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = ptx::smem_addr(smem_raw);
@@ -273,6 +288,10 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
       if (lane == 0) {
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
+        if constexpr (kAcc) {
+          ptx::prefetch_tensormap(&tm_kl);
+          ptx::prefetch_tensormap(&tm_vl);
+        }
         int64_t k_issued = 0, v_issued = 0;
         bool ok = true;
         for (int i = 0; ok && i < n_mine; ++i) {
@@ -282,16 +301,26 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
             const int st = kv_stage(g);
             const uint32_t free_par = kv_phase(g) ^ 1u;
             if (!(ok = w.wait(bar(kBarKEmpty + st), free_par, kSiteProducerK))) break;
-            ptx::mbar_arrive_expect_tx(bar(kBarKFull + st), tile_bytes);
-            for (int kb = 0; kb < NKB; ++kb)
-              ptx::tma_load_3d(base_s + P::kOffK + st * P::kTileF16 + kb * kBoxBytes, &tm_k,
+            ptx::mbar_arrive_expect_tx(bar(kBarKFull + st), P::kParts * tile_bytes);
+            for (int kb = 0; kb < NKB; ++kb) {
+              ptx::tma_load_3d(base_s + P::kOffK + st * P::kStageStride + kb * kBoxBytes, &tm_k,
                                bar(kBarKFull + st), kb * 64, j * kBN, bh);
+              if constexpr (kAcc)
+                ptx::tma_load_3d(base_s + P::kOffK + st * P::kStageStride + P::kPartBytes +
+                                     kb * kBoxBytes,
+                                 &tm_kl, bar(kBarKFull + st), kb * 64, j * kBN, bh);
+            }
             ++k_issued;
             if (!(ok = w.wait(bar(kBarVEmpty + st), free_par, kSiteProducerV))) break;
-            ptx::mbar_arrive_expect_tx(bar(kBarVFull + st), tile_bytes);
-            for (int kb = 0; kb < NKB; ++kb)
-              ptx::tma_load_3d(base_s + P::kOffV + st * P::kTileF16 + kb * kBoxBytes, &tm_v,
+            ptx::mbar_arrive_expect_tx(bar(kBarVFull + st), P::kParts * tile_bytes);
+            for (int kb = 0; kb < NKB; ++kb) {
+              ptx::tma_load_3d(base_s + P::kOffV + st * P::kStageStride + kb * kBoxBytes, &tm_v,
                                bar(kBarVFull + st), kb * 64, j * kBN, bh);
+              if constexpr (kAcc)
+                ptx::tma_load_3d(base_s + P::kOffV + st * P::kStageStride + P::kPartBytes +
+                                     kb * kBoxBytes,
+                                 &tm_vl, bar(kBarVFull + st), kb * 64, j * kBN, bh);
+            }
             ++v_issued;
           }
         }
@@ -307,15 +336,22 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
       // have read the previous ones.
       if (lane == 0) {
         ptx::prefetch_tensormap(&tm_q);
+        if constexpr (kAcc) ptx::prefetch_tensormap(&tm_ql);
         int q_issued = 0;
         for (int i = 0; i < n_mine; ++i) {
           if (i > 0 && !w.wait(bar(kBarQEmpty), static_cast<uint32_t>(i - 1) & 1u, kSiteProducerQ))
             break;
-          ptx::mbar_arrive_expect_tx(bar(kBarQFull), NQ * tile_bytes);
+          ptx::mbar_arrive_expect_tx(bar(kBarQFull), NQ * P::kParts * tile_bytes);
           for (int t = 0; t < NQ; ++t)
-            for (int kb = 0; kb < NKB; ++kb)
-              ptx::tma_load_3d(base_s + P::kOffQ + t * P::kTileF16 + kb * kBoxBytes, &tm_q,
+            for (int kb = 0; kb < NKB; ++kb) {
+              ptx::tma_load_3d(base_s + P::kOffQ + t * P::kStageStride + kb * kBoxBytes, &tm_q,
                                bar(kBarQFull), kb * 64, tile_row0(i) + t * kBM, tile_bh(i));
+              if constexpr (kAcc)
+                ptx::tma_load_3d(base_s + P::kOffQ + t * P::kStageStride + P::kPartBytes +
+                                     kb * kBoxBytes,
+                                 &tm_ql, bar(kBarQFull), kb * 64, tile_row0(i) + t * kBM,
+                                 tile_bh(i));
+            }
           ++q_issued;
         }
         if (q_issued > 0)
@@ -331,14 +367,21 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
         const uint32_t idesc_s = ptx::idesc_f16_f32(kBM, kBN, false);
         const int ksteps = p.d_pad >> 4;
         auto issue_s = [&](int t, int64_t g) {
-          const uint32_t qa = base_s + P::kOffQ + t * P::kTileF16;
-          const uint32_t kb = base_s + P::kOffK + kv_stage(g) * P::kTileF16;
+          const uint32_t qa = base_s + P::kOffQ + t * P::kStageStride;
+          const uint32_t kb = base_s + P::kOffK + kv_stage(g) * P::kStageStride;
           const uint32_t d = tmem + static_cast<uint32_t>(sbuf(t, g)) * 128u;
           for (int ks = 0; ks < ksteps; ++ks) {
             const uint32_t off = static_cast<uint32_t>((ks >> 2) * kBoxBytes + (ks & 3) * 32);
             ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
                         ptx::smem_desc(kb + off, 16, 1024, ptx::kSwizzle128B), idesc_s,
                         ks > 0 ? 1u : 0u);
+            if constexpr (kAcc) {  // + Qh Kl^T + Ql Kh^T
+              ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
+                          ptx::smem_desc(kb + P::kPartBytes + off, 16, 1024, ptx::kSwizzle128B),
+                          idesc_s, 1u);
+              ptx::mma_ss(d, ptx::smem_desc(qa + P::kPartBytes + off, 16, 1024, ptx::kSwizzle128B),
+                          ptx::smem_desc(kb + off, 16, 1024, ptx::kSwizzle128B), idesc_s, 1u);
+            }
           }
           ptx::mma_commit(bar(kBarSFull + sbuf(t, g)));
         };
@@ -366,13 +409,22 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
         // O_t += P_t V_g
         const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
         auto issue_pv = [&](int t, int64_t g, bool first) {
-          const uint32_t vb = base_s + P::kOffV + kv_stage(g) * P::kTileF16;
+          const uint32_t vb = base_s + P::kOffV + kv_stage(g) * P::kStageStride;
           const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
           const uint32_t a = tmem + P::kColP + static_cast<uint32_t>(t) * P::kColStride;
           for (int ks = 0; ks < kBN / 16; ++ks) {
             ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
                         ptx::smem_desc(vb + ks * 2048, kBoxBytes, 1024, ptx::kSwizzle128B),
                         idesc_pv, (!first || ks > 0) ? 1u : 0u);
+            if constexpr (kAcc) {  // + Ph Vl + Pl Vh
+              ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
+                          ptx::smem_desc(vb + P::kPartBytes + ks * 2048, kBoxBytes, 1024,
+                                         ptx::kSwizzle128B),
+                          idesc_pv, 1u);
+              ptx::mma_ts(d, tmem + P::kColPlo + static_cast<uint32_t>(ks) * 8u,
+                          ptx::smem_desc(vb + ks * 2048, kBoxBytes, 1024, ptx::kSwizzle128B),
+                          idesc_pv, 1u);
+            }
           }
           ptx::mma_commit(bar(kBarODone + t));
         };
@@ -452,6 +504,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
         uint32_t pk[4][16];
+        uint32_t pkl[kAcc ? 4 : 1][16];  // accurate mode: P lo = f16(p - f32(P hi))
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -462,6 +515,10 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
             const float2 pp = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
             acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
             pk[c][e] = ptx::pack_half2(pp.x, pp.y);
+            if constexpr (kAcc) {
+              const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&pk[c][e]));
+              pkl[c][e] = ptx::pack_half2(pp.x - back.x, pp.y - back.y);
+            }
           }
         }
         const float2 s01 = __fadd2_rn(acc[0], acc[1]);
@@ -487,6 +544,11 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk[c]);
+        if constexpr (kAcc) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            ptx::tmem_st_32x32b_x16(tmem + lane_addr + P::kColPlo + c * 16, pkl[c]);
+        }
 
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -501,7 +563,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
         break;
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
-      if (NKB == 1 && p.tma_out) {
+      if (P::kEpiBytes > 0 && p.tma_out) {
         // 16 columns at a time: TMEM -> registers -> swizzled shared buffer
         // -> one TMA store of the warp's 32 rows (rows past n_patches and
         // columns past head_dim are not written); the stores complete in
@@ -605,7 +667,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB>::kThreads, 1)
       ptx::tc_fence_before();
     }
     // the output stores must have completed before the block exits
-    if (NKB == 1 && p.tma_out && lane == 0) ptx::bulk_wait_group_all();
+    if (P::kEpiBytes > 0 && p.tma_out && lane == 0) ptx::bulk_wait_group_all();
   }
 
   ptx::tc_fence_before();

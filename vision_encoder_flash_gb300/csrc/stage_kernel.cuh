@@ -64,3 +64,55 @@ __global__ void __launch_bounds__(256) vattn_stage_kernel(StageJob a, StageJob b
 }
 
 }  // namespace vattn
+
+namespace vattn {
+
+// Two-term f16 split of q, k and v for the accurate mode:
+//   hi = f16(x), lo = f16(x - f32(hi))   (round to nearest even both times)
+// so x = hi + lo to about 2^-22 relative (f16 subnormals bound lo's error
+// at 2^-25 absolute).  Same layout and chunk decomposition as
+// vattn_stage_kernel; `dst` of each job receives hi, `dst_lo` lo.
+struct SplitJob {
+  const float* src;
+  __half* dst;
+  __half* dst_lo;
+};
+
+__global__ void __launch_bounds__(256) vattn_stage_split_kernel(SplitJob a, SplitJob b, SplitJob c,
+                                                               long long n_rows, int D, int d_pad,
+                                                               int vec) {
+  const int cpr = d_pad >> 3;
+  const long long chunks_per_tensor = n_rows * cpr;
+  const long long total = 3 * chunks_per_tensor;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int which = static_cast<int>(i / chunks_per_tensor);
+    const long long r = i - which * chunks_per_tensor;
+    const long long row = r / cpr;
+    const int ch = static_cast<int>(r - row * cpr);
+    const SplitJob job = which == 0 ? a : (which == 1 ? b : c);
+    const float* s = job.src + row * D + ch * 8;
+    float x[8];
+    if (vec && ch * 8 + 8 <= D) {
+      const float4 lo = __ldg(reinterpret_cast<const float4*>(s));
+      const float4 hi = __ldg(reinterpret_cast<const float4*>(s) + 1);
+      x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+      x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = (ch * 8 + e < D) ? __ldg(s + e) : 0.0f;
+    }
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      h[e] = ptx::pack_half2(x[2 * e], x[2 * e + 1]);
+      const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
+      l[e] = ptx::pack_half2(x[2 * e] - back.x, x[2 * e + 1] - back.y);
+    }
+    *reinterpret_cast<uint4*>(job.dst + row * d_pad + ch * 8) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(job.dst_lo + row * d_pad + ch * 8) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+}  // namespace vattn

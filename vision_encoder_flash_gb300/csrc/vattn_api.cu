@@ -160,12 +160,16 @@ vattn_status sm_count(int device, int* out) {
 
 // The attention kernel is persistent: one block per multiprocessor (at most
 // one per tile), each looping over the tiles blockIdx.x + k * gridDim.x.
-template <int NQ, int NKB, bool kOut16 = false>
-vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              vattn::Params p, unsigned n_tiles, cudaStream_t stream,
-                              int device) {
-  using P = vattn::Plan<NQ, NKB>;
-  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kOut16>;
+// tql, tkl, tvl: the lo halves of q, k, v (accurate mode only; otherwise
+// unused and any valid map may be passed).
+template <int NQ, int NKB, bool kOut16, bool kAcc>
+vattn_status launch_attention_maps(const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const CUtensorMap& tql,
+                                   const CUtensorMap& tkl, const CUtensorMap& tvl,
+                                   vattn::Params p, unsigned n_tiles, cudaStream_t stream,
+                                   int device) {
+  using P = vattn::Plan<NQ, NKB, kAcc>;
+  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kOut16, kAcc>;
   static std::atomic<uint8_t> configured[kMaxDevices];
   if (!configured[device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -182,17 +186,25 @@ vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, cons
   CUtensorMap to;
   std::memset(&to, 0, sizeof(to));
   p.tma_out = 0;
-  if (NKB == 1 && p.vec_out) {
+  if (P::kEpiBytes > 0 && p.vec_out) {
     void* out_base = kOut16 ? static_cast<void*>(p.out16) : static_cast<void*>(p.out);
     const vattn_status so = make_tmap_out(&to, out_base, static_cast<int64_t>(p.n_tiles / p.n_qblocks),
                                           p.n_patches, p.head_dim, kOut16);
     if (so != VATTN_OK) return so;
     p.tma_out = 1;
   }
-  kernel<<<grid, P::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, to, p);
+  kernel<<<grid, P::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, to, tql, tkl, tvl, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   return VATTN_OK;
+}
+
+template <int NQ, int NKB, bool kOut16 = false>
+vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              vattn::Params p, unsigned n_tiles, cudaStream_t stream,
+                              int device) {
+  return launch_attention_maps<NQ, NKB, kOut16, false>(tq, tk, tv, tq, tk, tv, p, n_tiles,
+                                                       stream, device);
 }
 
 // Arguments of the NeoX rotation (checked on the host, before any CUDA call).
@@ -572,6 +584,96 @@ vattn_status vattn_forward_rope(const float* q, const float* k, const float* v, 
         st = launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
       else
         st = launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+    }
+  }
+  e = cudaFreeAsync(ws, stream);
+  if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
+  return st;
+}
+
+vattn_status vattn_forward_accurate(const float* q, const float* k, const float* v, float* out,
+                                    int64_t batch, int64_t n_heads, int64_t n_patches,
+                                    int64_t head_dim, void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks: those of vattn_forward
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
+                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (head_dim > VATTN_MAX_HEAD_DIM)
+    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
+  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
+  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+
+  const int D = static_cast<int>(head_dim);
+  const int N = static_cast<int>(n_patches);
+  const int d_pad = (D + 15) & ~15;
+  const int nkb = d_pad <= 64 ? 1 : 2;
+  const int64_t n_qblocks = (N + vattn::kBM - 1) / vattn::kBM;  // one query tile per work tile
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+  vattn::Params p{};
+  p.out = out;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = d_pad;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+
+  // ---- device side: workspace = f16 hi and lo copies of q, k, v
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int64_t rows = bh * N;
+  const size_t region = (static_cast<size_t>(rows) * d_pad * 2 + 255) & ~static_cast<size_t>(255);
+  cudaMemPool_t pool = nullptr;
+  vattn_status st = pool_for(device, &pool);
+  if (st != VATTN_OK) return st;
+  void* ws = nullptr;
+  e = cudaMallocFromPoolAsync(&ws, 6 * region, pool, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  __half* part[6];
+  for (int i = 0; i < 6; ++i)
+    part[i] = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + i * region);
+  CUtensorMap tm[6];
+  for (int i = 0; i < 6 && st == VATTN_OK; ++i) st = make_tmap16(&tm[i], part[i], bh, N, d_pad);
+  if (st == VATTN_OK) {
+    const int vec = (D % 8 == 0) &&
+                    ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                      reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+    const long long chunks = 3LL * rows * (d_pad / 8);
+    const long long blocks = (chunks + 255) / 256;
+    const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
+    vattn::vattn_stage_split_kernel<<<stage_grid, 256, 0, stream>>>(
+        vattn::SplitJob{q, part[0], part[3]}, vattn::SplitJob{k, part[1], part[4]},
+        vattn::SplitJob{v, part[2], part[5]}, rows, D, d_pad, vec);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "staging kernel launch");
+    } else {
+      const unsigned g = static_cast<unsigned>(grid);
+      if (nkb == 1)
+        st = launch_attention_maps<1, 1, false, true>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], p,
+                                                      g, stream, device);
+      else
+        st = launch_attention_maps<1, 2, false, true>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], p,
+                                                      g, stream, device);
     }
   }
   e = cudaFreeAsync(ws, stream);
