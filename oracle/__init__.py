@@ -11,6 +11,9 @@ It restates, in plain f64 C (``vattn_oracle.c``), what the WGSL shader
 
 ``oracle.rope`` (plain NumPy, f64) restates the NeoX rotary embedding of the
 WGSL kernel "rope_neox_backward.wgsl" (rullama 0.2.0), forward and inverse.
+
+``oracle.conv1d`` (plain NumPy, f64) restates the depthwise conv1d
+rolling-buffer step of the WGSL kernel "conv1d.wgsl" (cera 0.2.0).
 """
 from __future__ import annotations
 
