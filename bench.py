@@ -486,6 +486,7 @@ def run_vattn(args, workload):
                              "what": "vattn_rope_neox on q, k, v stacked (f32, in place, 226 MB > L2), includes the angle-table kernel"},
         }
         del xr
+        variants["conv1d_step"] = conv1d_variant(torch, dev, stream, float(pk["hbm_gbs"]))
 
     if rank != 0:
         if pg is not None:
@@ -528,6 +529,43 @@ def run_vattn(args, workload):
     return 0
 
 
+def conv1d_variant(torch, dev, stream, hbm_gbs):
+    """The depthwise conv1d rolling-buffer step on its workload: two input
+    sets used in turn (each 268 MB, so a step never finds the previous
+    step's data in the 129 MB L2), CUDA events around 200 launches."""
+    import vision_encoder_flash_gb300 as vef
+    from vattn_inputs import CONV1D_WORKLOAD as wl, conv1d_inputs, conv1d_workload_name
+
+    B, H, K, DC = wl["batch"], wl["hidden"], wl["kernel_size"], wl["d_conv"]
+    sets = []
+    for i in range(2):
+        x, buf, w = conv1d_inputs(B, H, K, DC, wl["seed"] + i)
+        sets.append(tuple(torch.from_numpy(a).to(dev) for a in (x, buf, w)) +
+                    (torch.empty(B, H, device=dev),))
+    reps = 200
+    for i in range(10):
+        x, buf, w, o = sets[i & 1]
+        vef.conv1d_step(x, buf, w, out=o, stream=stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for i in range(reps):
+        x, buf, w, o = sets[i & 1]
+        vef.conv1d_step(x, buf, w, out=o, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / reps
+    nbytes = B * H * (2 * DC + 2) * 4 + H * K * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del sets
+    return {"workload": conv1d_workload_name(), "ms": round(ms, 5), "bytes": nbytes,
+            "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_gbs, 4),
+            "bound": "hbm", "launches_timed": reps,
+            "what": "vattn_conv1d_step: (2 d_conv + 2) * 4 algorithmic bytes per (sequence, channel) "
+                    "(buffer read and rewritten, input read, output written) + the weights once; "
+                    "two input sets in turn, larger than L2"}
+
+
 def main(argv=None):
     from vattn_inputs import WORKLOADS
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -538,6 +576,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=5, choices=sorted(WORKLOADS))
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--conv1d-only", action="store_true",
+                    help="time only the conv1d rolling-buffer step and print its line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -548,6 +588,17 @@ def main(argv=None):
     workload = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, workload)
+    if args.conv1d_only:
+        import torch
+        import vision_encoder_flash_gb300 as vef
+        from vision_encoder_flash_gb300 import build
+        build.build()
+        vef.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        line = conv1d_variant(torch, dev, torch.cuda.current_stream(dev), float(peaks()[0]["hbm_gbs"]))
+        print(json.dumps(line))
+        return 0
     return run_vattn(args, workload)
 
 

@@ -186,6 +186,44 @@ vattn_status vattn_forward_accurate(const float* q, const float* k, const float*
                                     int64_t head_dim, void* stream);
 
 /*
+ * vattn_conv1d_step -- one step of a depthwise (per-channel) causal conv1d
+ * whose past inputs live in a rolling buffer, for a batch of independent
+ * sequences: the WGSL kernel "conv1d.wgsl" (cera 0.2.0), its header comment
+ * and bindings.  For every sequence b and channel ch:
+ *
+ *   output[b, ch] = sum_{k < d_conv} buffer[b, k, ch] * weight[ch, k]
+ *                   + input[b, ch] * weight[ch, d_conv]
+ *
+ * in f32, taps in that order, each product-and-add one fused multiply-add;
+ * then, in place, buffer[b, k, ch] <- buffer[b, k + 1, ch] for
+ * k < d_conv - 1 and buffer[b, d_conv - 1, ch] <- input[b, ch] (slot 0 is
+ * the oldest).  With batch == 1 this is exactly the page's kernel.
+ *
+ * input, output: DEVICE pointers to f32 [batch, hidden_size].
+ * buffer: DEVICE pointer to f32 [batch, d_conv, hidden_size] (each
+ *   sequence's block is the page's [d_conv, hidden_size] layout, slot k of
+ *   channel ch at k * hidden_size + ch), read and rewritten; may be NULL
+ *   when d_conv == 0.
+ * weight: DEVICE pointer to f32 [hidden_size, kernel_size], tap k of
+ *   channel ch at ch * kernel_size + k, shared by all sequences; taps past
+ *   d_conv are not read.  kernel_size >= d_conv + 1.
+ * All 4-byte aligned (hidden_size % 4 == 0, d_conv <= 8 and 16-byte aligned
+ * input, buffer and output take 16-byte accesses).  output must not overlap
+ * input, buffer or weight; buffer must not overlap input or weight.  The
+ * caller owns all buffers.
+ *
+ * Asynchronous on `stream`, one kernel launch, no allocation; batch == 0 or
+ * hidden_size == 0 is a no-op.  Calls that update one buffer must be
+ * ordered (one stream, or events).  Argument errors are returned before any
+ * CUDA call: VATTN_ERR_INVALID_ARG (negative size, kernel_size < d_conv + 1,
+ * null pointer, overlap), VATTN_ERR_UNSUPPORTED (sizes past 32 bits or byte
+ * sizes past 64), VATTN_ERR_MISALIGNED; VATTN_ERR_CUDA if the launch fails.
+ */
+vattn_status vattn_conv1d_step(const float* input, float* buffer, const float* weight,
+                               float* output, int64_t batch, int64_t hidden_size,
+                               int64_t kernel_size, int64_t d_conv, void* stream);
+
+/*
  * Size of the fixed staging scratch of vattn_forward_noalloc: 32 MiB, enough
  * for batch*n_heads*n_patches*round_up(head_dim, 16) <= 5,592,320 (for
  * example 16 heads x 4,100 patches at head_dim 72, or 64 heads x 1,024

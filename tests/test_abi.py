@@ -20,6 +20,7 @@ def test_exports_every_declared_symbol(lib):
     names = _lib.exported_symbols()
     assert set(names) == {"vattn_forward", "vattn_forward_f16", "vattn_forward_f16io",
                           "vattn_forward_noalloc", "vattn_forward_accurate",
+                          "vattn_conv1d_step",
                           "vattn_rope_neox", "vattn_forward_rope",
                           "vattn_device_status", "vattn_status_string",
                           "vattn_last_error_string", "vattn_version"}
@@ -122,6 +123,48 @@ def test_empty_problems_are_no_ops_even_with_null_pointers(lib, b, h, n):
     assert _lib.forward_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
     assert _lib.forward_noalloc_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
     assert _lib.forward_accurate_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
+
+
+B4 = FAKE + 2 ** 24   # buffer
+W4 = FAKE + 2 ** 28   # weight
+O4 = FAKE + 2 ** 32   # output
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, B4, W4, O4, -1, 8, 3, 2), 1),
+    ((FAKE, B4, W4, O4, 1, -8, 3, 2), 1),
+    ((FAKE, B4, W4, O4, 1, 8, 3, -1), 1),
+    ((FAKE, B4, W4, O4, 1, 8, 2, 2), 1),          # kernel_size < d_conv + 1
+    ((FAKE, B4, W4, O4, 1, 8, 0, 0), 1),          # kernel_size 0: no input tap
+    ((0, B4, W4, O4, 1, 8, 3, 2), 1),
+    ((FAKE, 0, W4, O4, 1, 8, 3, 2), 1),           # buffer needed when d_conv > 0
+    ((FAKE, B4, 0, O4, 1, 8, 3, 2), 1),
+    ((FAKE, B4, W4, 0, 1, 8, 3, 2), 1),
+    ((FAKE + 2, B4, W4, O4, 1, 8, 3, 2), 3),
+    ((FAKE, B4 + 1, W4, O4, 1, 8, 3, 2), 3),
+    ((FAKE, B4, W4, FAKE + 16, 1, 8, 3, 2), 1),   # output overlaps input
+    ((FAKE, B4, W4, B4 + 32, 1, 8, 3, 2), 1),     # output overlaps buffer
+    ((FAKE, B4, W4, W4, 1, 8, 3, 2), 1),          # output overlaps weight
+    ((FAKE, FAKE + 8, W4, O4, 1, 8, 3, 2), 1),    # buffer overlaps input
+    ((FAKE, B4, B4 + 60, O4, 1, 8, 3, 2), 1),     # buffer (64 B) overlaps weight
+    ((FAKE, B4, W4, O4, 1, 2 ** 31, 3, 2), 2),
+    ((FAKE, B4, W4, O4, 2 ** 62, 2 ** 20, 3, 2), 2),
+])
+def test_conv1d_host_side_argument_errors(lib, args, status):
+    assert _lib.conv1d_step_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""
+
+
+@pytest.mark.parametrize("b,h", [(0, 16), (3, 0)])
+def test_conv1d_empty_problems_are_no_ops(lib, b, h):
+    assert _lib.conv1d_step_status(0, 0, 0, 0, b, h, 4, 3, 0) == 0
+
+
+def test_conv1d_without_buffer_slots_needs_no_buffer(lib):
+    # d_conv == 0 accepts a NULL buffer; this still fails later only for the
+    # missing input, before any CUDA call
+    assert _lib.conv1d_step_status(0, 0, W4, O4, 1, 8, 1, 0, 0) == 1
+    assert "null" in lib.vattn_last_error_string().decode()
 
 
 def test_python_binding_rejects_bad_tensors():

@@ -15,6 +15,16 @@ Recipe (the workloads of the vision-attention shader: image patches, head-major
   ``offset[h]`` drawn from N(0, 2) (variance 2, standard deviation sqrt(2)),
   shared across the batch and across rows;
 * every array is cast to float32 once, at the end.
+
+The depthwise conv1d rolling-buffer step (page "conv1d.wgsl", cera 0.2.0)
+has its own recipe, ``conv1d_inputs``: the same generator, drawing input
+``[batch, hidden]``, buffer ``[batch, d_conv, hidden]`` (both
+``standard_normal``) and weight ``[hidden, kernel_size]``
+(``standard_normal / sqrt(d_conv + 1)``, so an output has unit variance), in
+that order, cast to float32 at the end.  The page gives no sizes; the
+benchmark workload ``CONV1D_WORKLOAD`` is a decode step of 8192 sequences
+with 2048 channels and a 3-tap kernel (2 buffer slots): 403 MB moved per
+step, three times the 129 MB L2.
 """
 from __future__ import annotations
 
@@ -85,3 +95,19 @@ def workload_inputs(index: int):
     w = WORKLOADS[index]
     return make_inputs(w.batch, w.n_heads, w.n_patches, w.head_dim, w.seed,
                        w.peaked)
+
+
+CONV1D_WORKLOAD = dict(batch=8192, hidden=2048, kernel_size=3, d_conv=2, seed=SEED_BASE + 40)
+
+
+def conv1d_workload_name(w=CONV1D_WORKLOAD) -> str:
+    return f"conv1d_step_b{w['batch']}_h{w['hidden']}_k{w['kernel_size']}_dc{w['d_conv']}"
+
+
+def conv1d_inputs(batch: int, hidden: int, kernel_size: int, d_conv: int, seed: int):
+    """Return float32 ``(input, buffer, weight)`` for the conv1d step."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal((batch, hidden))
+    buf = rng.standard_normal((batch, d_conv, hidden))
+    w = rng.standard_normal((hidden, kernel_size)) / np.sqrt(d_conv + 1)
+    return x.astype(np.float32), buf.astype(np.float32), w.astype(np.float32)

@@ -9,12 +9,13 @@ missing or no GPU is present the calls raise.
 """
 from __future__ import annotations
 
-from ._lib import (VattnError, _check, device_status, exported_symbols, forward_accurate_status,
+from ._lib import (VattnError, _check, conv1d_step_status, device_status, exported_symbols,
+                   forward_accurate_status,
                    forward_f16_raw, forward_f16io_status,
                    forward_noalloc_raw, forward_raw, forward_rope_status, lib_path,
                    load_library, rope_neox_status, status_string, version)
 
-__all__ = ["forward", "forward_accurate", "forward_f16", "forward_f16io", "forward_rope", "rope_neox", "forward_raw",
+__all__ = ["forward", "forward_accurate", "conv1d_step", "forward_f16", "forward_f16io", "forward_rope", "rope_neox", "forward_raw",
            "forward_f16_raw", "forward_noalloc_raw",
            "device_status", "VattnError", "load_library",
            "lib_path", "exported_symbols", "status_string", "version"]
@@ -210,6 +211,40 @@ def forward_accurate(q, k, v, out=None, stream=None):
     B, H, N, D = q.shape
     _check(forward_accurate_status(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
                                    N, D, s.cuda_stream))
+    return out
+
+
+def conv1d_step(input, buffer, weight, out=None, stream=None):
+    """One depthwise conv1d rolling-buffer step on CUDA f32 tensors.
+
+    input ``[batch, hidden]`` (or ``[hidden]``), buffer ``[batch, d_conv,
+    hidden]`` (or ``[d_conv, hidden]``, updated in place), weight
+    ``[hidden, kernel_size]`` with ``kernel_size >= d_conv + 1``.  Returns
+    ``out`` (shape of input) without synchronising."""
+    import torch
+
+    for name, t in (("input", input), ("buffer", buffer), ("weight", weight)):
+        _cuda_f32(name, t)
+    single = input.dim() == 1
+    x = input.unsqueeze(0) if single else input
+    buf = buffer.unsqueeze(0) if single else buffer
+    if x.dim() != 2 or buf.dim() != 3 or weight.dim() != 2:
+        raise ValueError("expected input [B, hidden], buffer [B, d_conv, hidden], weight [hidden, K]")
+    B, hidden = x.shape
+    d_conv = buf.shape[1]
+    if tuple(buf.shape) != (B, d_conv, hidden) or weight.shape[0] != hidden:
+        raise ValueError(f"shape mismatch: input {tuple(input.shape)}, buffer {tuple(buffer.shape)}, "
+                         f"weight {tuple(weight.shape)}")
+    if not (input.device == buffer.device == weight.device):
+        raise ValueError("input, buffer and weight must be on one device")
+    if out is None:
+        out = torch.empty_like(input)
+    _cuda_f32("out", out)
+    if out.shape != input.shape or out.device != input.device:
+        raise ValueError("out must match input in shape and device")
+    s = stream if stream is not None else torch.cuda.current_stream(input.device)
+    _check(conv1d_step_status(x.data_ptr(), buf.data_ptr(), weight.data_ptr(), out.data_ptr(), B,
+                              hidden, weight.shape[1], d_conv, s.cuda_stream))
     return out
 
 

@@ -49,6 +49,8 @@ def load_library():
     lib.vattn_forward_f16.restype = ctypes.c_int
     lib.vattn_forward_accurate.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_accurate.restype = ctypes.c_int
+    lib.vattn_conv1d_step.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.vattn_conv1d_step.restype = ctypes.c_int
     lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_noalloc.restype = ctypes.c_int
     lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -126,6 +128,13 @@ def forward_accurate_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patc
     addresses; returns the status code."""
     return int(load_library().vattn_forward_accurate(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                                      n_patches, head_dim, stream))
+
+
+def conv1d_step_status(input_ptr, buffer_ptr, weight_ptr, output_ptr, batch, hidden_size,
+                       kernel_size, d_conv, stream=0) -> int:
+    """vattn_conv1d_step with device addresses; returns the status code."""
+    return int(load_library().vattn_conv1d_step(input_ptr, buffer_ptr, weight_ptr, output_ptr, batch,
+                                                hidden_size, kernel_size, d_conv, stream))
 
 
 def forward_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int,

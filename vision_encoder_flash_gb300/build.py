@@ -17,6 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "vattn_api.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "attn_kernel.cuh"), os.path.join(CSRC, "stage_kernel.cuh"),
                   os.path.join(CSRC, "rope_kernel.cuh"),
+                  os.path.join(CSRC, "conv1d_kernel.cuh"),
                   os.path.join(CSRC, "ptx.cuh"),
                   os.path.join(ROOT, "include", "vattn.h")]
 LIB = os.path.join(PKG, "libvattn.so")

@@ -19,6 +19,7 @@
 
 #include "../../include/vattn.h"
 #include "attn_kernel.cuh"
+#include "conv1d_kernel.cuh"
 #include "rope_kernel.cuh"
 #include "stage_kernel.cuh"
 
@@ -679,6 +680,79 @@ vattn_status vattn_forward_accurate(const float* q, const float* k, const float*
   e = cudaFreeAsync(ws, stream);
   if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
   return st;
+}
+
+vattn_status vattn_conv1d_step(const float* input, float* buffer, const float* weight,
+                               float* output, int64_t batch, int64_t hidden_size,
+                               int64_t kernel_size, int64_t d_conv, void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks, before any CUDA call
+  if (batch < 0 || hidden_size < 0 || kernel_size < 0 || d_conv < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld hidden_size=%lld kernel_size=%lld d_conv=%lld)",
+                (long long)batch, (long long)hidden_size, (long long)kernel_size, (long long)d_conv);
+  if (kernel_size < d_conv + 1)
+    return fail(VATTN_ERR_INVALID_ARG, "kernel_size %lld < d_conv + 1 = %lld (tap d_conv weighs the input)",
+                (long long)kernel_size, (long long)d_conv + 1);
+  if (hidden_size > INT32_MAX || kernel_size > INT32_MAX || d_conv > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "hidden_size, kernel_size and d_conv must fit in 32 bits");
+  if (batch == 0 || hidden_size == 0) return VATTN_OK;  // nothing to compute
+  if (!input || !weight || !output || (d_conv > 0 && !buffer))
+    return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (batch > INT64_MAX / 4 / hidden_size / (d_conv + 1) || hidden_size > INT64_MAX / 4 / kernel_size)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t row_bytes = static_cast<uint64_t>(batch) * hidden_size * 4u;
+  const uint64_t buf_bytes = row_bytes * static_cast<uint64_t>(d_conv);
+  const uint64_t w_bytes = static_cast<uint64_t>(hidden_size) * kernel_size * 4u;
+  const uintptr_t align_or = reinterpret_cast<uintptr_t>(input) | reinterpret_cast<uintptr_t>(buffer) |
+                             reinterpret_cast<uintptr_t>(weight) | reinterpret_cast<uintptr_t>(output);
+  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
+  if (overlaps2(output, row_bytes, input, row_bytes) || overlaps2(output, row_bytes, weight, w_bytes) ||
+      (d_conv > 0 && overlaps2(output, row_bytes, buffer, buf_bytes)))
+    return fail(VATTN_ERR_INVALID_ARG, "output overlaps input, buffer or weight");
+  if (d_conv > 0 && (overlaps2(buffer, buf_bytes, input, row_bytes) ||
+                     overlaps2(buffer, buf_bytes, weight, w_bytes)))
+    return fail(VATTN_ERR_INVALID_ARG, "buffer overlaps input or weight");
+
+  // ---- device side: one streaming kernel
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int sms = 0;
+  const vattn_status st = sm_count(device, &sms);
+  if (st != VATTN_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  vattn::Conv1dArgs a{input, buffer, weight, output, static_cast<long long>(batch),
+                      static_cast<int>(hidden_size), static_cast<int>(kernel_size),
+                      static_cast<int>(d_conv)};
+  // 8 blocks of 256 threads per multiprocessor (full occupancy), fewer for
+  // small problems; the kernels loop over the rest
+  auto grid_for = [sms](long long items) {
+    const long long blocks = (items + 255) / 256;
+    const long long cap = 8LL * sms;
+    return static_cast<unsigned>(blocks < cap ? blocks : cap);
+  };
+  const bool by4 = (hidden_size % 4 == 0) && d_conv <= 8 &&
+                   ((reinterpret_cast<uintptr_t>(input) | reinterpret_cast<uintptr_t>(buffer) |
+                     reinterpret_cast<uintptr_t>(output)) & 15u) == 0;
+  if (by4) {
+    const unsigned g = grid_for(batch * (hidden_size / 4));
+    switch (d_conv) {
+      case 0: vattn::vattn_conv1d_step4_kernel<0><<<g, 256, 0, stream>>>(a); break;
+      case 1: vattn::vattn_conv1d_step4_kernel<1><<<g, 256, 0, stream>>>(a); break;
+      case 2: vattn::vattn_conv1d_step4_kernel<2><<<g, 256, 0, stream>>>(a); break;
+      case 3: vattn::vattn_conv1d_step4_kernel<3><<<g, 256, 0, stream>>>(a); break;
+      case 4: vattn::vattn_conv1d_step4_kernel<4><<<g, 256, 0, stream>>>(a); break;
+      case 5: vattn::vattn_conv1d_step4_kernel<5><<<g, 256, 0, stream>>>(a); break;
+      case 6: vattn::vattn_conv1d_step4_kernel<6><<<g, 256, 0, stream>>>(a); break;
+      case 7: vattn::vattn_conv1d_step4_kernel<7><<<g, 256, 0, stream>>>(a); break;
+      default: vattn::vattn_conv1d_step4_kernel<8><<<g, 256, 0, stream>>>(a); break;
+    }
+  } else {
+    vattn::vattn_conv1d_step_kernel<<<grid_for(batch * hidden_size), 256, 0, stream>>>(a);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d kernel launch");
+  return VATTN_OK;
 }
 
 vattn_status vattn_device_status(uint32_t* code) {
