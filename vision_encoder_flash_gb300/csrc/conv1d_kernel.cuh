@@ -34,7 +34,11 @@ struct Conv1dArgs {
 // Four consecutive channels per thread with 16-byte loads and stores;
 // needs hidden % 4 == 0 and 16-byte aligned input, buffer and output.
 // DC = d_conv, fixed at compile time so the slots stay in registers.
-template <int DC>
+// kDense: kernel_size == d_conv + 1 and a 16-byte aligned weight, so a
+// thread's 4 (d_conv + 1) taps are contiguous and come in as d_conv + 1
+// 16-byte loads (4-byte loads at a lane stride of 16 (d_conv + 1) bytes hit
+// the same L1 banks and cost up to a third of the bandwidth at d_conv 3).
+template <int DC, bool kDense>
 __global__ void __launch_bounds__(256) vattn_conv1d_step4_kernel(const Conv1dArgs a) {
   const float* __restrict__ x_base = a.input;
   float* __restrict__ buf_base = a.buffer;
@@ -53,10 +57,25 @@ __global__ void __launch_bounds__(256) vattn_conv1d_step4_kernel(const Conv1dArg
     for (int k = 0; k < DC; ++k)
       s[k] = __ldcs(reinterpret_cast<const float4*>(buf_base + (b * DC + k) * a.hidden + ch));
     float w[4][DC + 1];
+    if constexpr (kDense) {
+      // taps of channels ch .. ch + 3: 4 (DC + 1) floats from ch * (DC + 1)
+      float flat[4 * (DC + 1)];
+      const float4* wq = reinterpret_cast<const float4*>(w_base + static_cast<long long>(ch) * (DC + 1));
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+      for (int i = 0; i < DC + 1; ++i) {
+        const float4 t = __ldg(wq + i);
+        flat[4 * i] = t.x; flat[4 * i + 1] = t.y; flat[4 * i + 2] = t.z; flat[4 * i + 3] = t.w;
+      }
 #pragma unroll
-      for (int k = 0; k <= DC; ++k) w[e][k] = __ldg(w_base + static_cast<long long>(ch + e) * ks + k);
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int k = 0; k <= DC; ++k) w[e][k] = flat[e * (DC + 1) + k];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int k = 0; k <= DC; ++k) w[e][k] = __ldg(w_base + static_cast<long long>(ch + e) * ks + k);
+    }
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int k = 0; k < DC; ++k) {

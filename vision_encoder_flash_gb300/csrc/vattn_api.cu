@@ -148,6 +148,7 @@ vattn_status pool_for(int device, cudaMemPool_t* out) {
 std::atomic<int> g_sm_count[kMaxDevices];
 
 vattn_status sm_count(int device, int* out) {
+  if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
   int n = g_sm_count[device].load(std::memory_order_acquire);
   if (n <= 0) {
     const cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
@@ -310,6 +311,51 @@ vattn_status forward_f16_impl(const uint16_t* q, const uint16_t* k, const uint16
   if (nkb == 1 && nq == 2) return launch_attention<2, 1, kOut16>(tq, tk, tv, p, g, stream, device);
   if (nkb == 1) return launch_attention<1, 1, kOut16>(tq, tk, tv, p, g, stream, device);
   return launch_attention<1, 2, kOut16>(tq, tk, tv, p, g, stream, device);
+}
+
+// Blocks of `threads` threads of `kernel` that fit on one multiprocessor,
+// looked up once per device (cache: one slot per device).
+template <typename Kernel>
+vattn_status resident_blocks(Kernel kernel, int threads, int device, std::atomic<int>* cache,
+                             int* out) {
+  int n = cache[device].load(std::memory_order_acquire);
+  if (n <= 0) {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (n <= 0) return fail(VATTN_ERR_CUDA, "kernel does not fit with %d threads per block", threads);
+    cache[device].store(n, std::memory_order_release);
+  }
+  *out = n;
+  return VATTN_OK;
+}
+
+// The conv1d kernels loop over their items: the grid is what fits on the
+// GPU at once (one wave; a grid past that leaves a partial second wave with
+// too few loads in flight), fewer blocks for small problems.
+template <typename Kernel>
+vattn_status launch_streaming(Kernel kernel, std::atomic<int>* cache, long long threads_wanted,
+                              const vattn::Conv1dArgs& a, int device, int sms,
+                              cudaStream_t stream) {
+  int per_sm = 0;
+  const vattn_status st = resident_blocks(kernel, 256, device, cache, &per_sm);
+  if (st != VATTN_OK) return st;
+  const long long blocks = (threads_wanted + 255) / 256;
+  const long long cap = static_cast<long long>(per_sm) * sms;
+  kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "conv1d kernel launch");
+  return VATTN_OK;
+}
+
+template <int DC>
+vattn_status launch_conv1d4(const vattn::Conv1dArgs& a, int device, int sms, cudaStream_t stream) {
+  static std::atomic<int> cache[2][kMaxDevices];
+  const long long items = a.batch * (a.hidden / 4);
+  if (a.kernel_size == DC + 1 && (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0)
+    return launch_streaming(vattn::vattn_conv1d_step4_kernel<DC, true>, cache[1], items, a, device,
+                            sms, stream);
+  return launch_streaming(vattn::vattn_conv1d_step4_kernel<DC, false>, cache[0], items, a, device,
+                          sms, stream);
 }
 
 }  // namespace
@@ -724,35 +770,25 @@ vattn_status vattn_conv1d_step(const float* input, float* buffer, const float* w
   vattn::Conv1dArgs a{input, buffer, weight, output, static_cast<long long>(batch),
                       static_cast<int>(hidden_size), static_cast<int>(kernel_size),
                       static_cast<int>(d_conv)};
-  // 8 blocks of 256 threads per multiprocessor (full occupancy), fewer for
-  // small problems; the kernels loop over the rest
-  auto grid_for = [sms](long long items) {
-    const long long blocks = (items + 255) / 256;
-    const long long cap = 8LL * sms;
-    return static_cast<unsigned>(blocks < cap ? blocks : cap);
-  };
   const bool by4 = (hidden_size % 4 == 0) && d_conv <= 8 &&
                    ((reinterpret_cast<uintptr_t>(input) | reinterpret_cast<uintptr_t>(buffer) |
                      reinterpret_cast<uintptr_t>(output)) & 15u) == 0;
-  if (by4) {
-    const unsigned g = grid_for(batch * (hidden_size / 4));
-    switch (d_conv) {
-      case 0: vattn::vattn_conv1d_step4_kernel<0><<<g, 256, 0, stream>>>(a); break;
-      case 1: vattn::vattn_conv1d_step4_kernel<1><<<g, 256, 0, stream>>>(a); break;
-      case 2: vattn::vattn_conv1d_step4_kernel<2><<<g, 256, 0, stream>>>(a); break;
-      case 3: vattn::vattn_conv1d_step4_kernel<3><<<g, 256, 0, stream>>>(a); break;
-      case 4: vattn::vattn_conv1d_step4_kernel<4><<<g, 256, 0, stream>>>(a); break;
-      case 5: vattn::vattn_conv1d_step4_kernel<5><<<g, 256, 0, stream>>>(a); break;
-      case 6: vattn::vattn_conv1d_step4_kernel<6><<<g, 256, 0, stream>>>(a); break;
-      case 7: vattn::vattn_conv1d_step4_kernel<7><<<g, 256, 0, stream>>>(a); break;
-      default: vattn::vattn_conv1d_step4_kernel<8><<<g, 256, 0, stream>>>(a); break;
-    }
-  } else {
-    vattn::vattn_conv1d_step_kernel<<<grid_for(batch * hidden_size), 256, 0, stream>>>(a);
+  if (!by4) {
+    static std::atomic<int> cache[kMaxDevices];
+    return launch_streaming(vattn::vattn_conv1d_step_kernel, cache, batch * hidden_size, a, device,
+                            sms, stream);
   }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "conv1d kernel launch");
-  return VATTN_OK;
+  switch (d_conv) {
+    case 0: return launch_conv1d4<0>(a, device, sms, stream);
+    case 1: return launch_conv1d4<1>(a, device, sms, stream);
+    case 2: return launch_conv1d4<2>(a, device, sms, stream);
+    case 3: return launch_conv1d4<3>(a, device, sms, stream);
+    case 4: return launch_conv1d4<4>(a, device, sms, stream);
+    case 5: return launch_conv1d4<5>(a, device, sms, stream);
+    case 6: return launch_conv1d4<6>(a, device, sms, stream);
+    case 7: return launch_conv1d4<7>(a, device, sms, stream);
+    default: return launch_conv1d4<8>(a, device, sms, stream);
+  }
 }
 
 vattn_status vattn_device_status(uint32_t* code) {
