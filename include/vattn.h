@@ -224,6 +224,36 @@ vattn_status vattn_conv1d_step(const float* input, float* buffer, const float* w
                                int64_t kernel_size, int64_t d_conv, void* stream);
 
 /*
+ * vattn_forward_host -- vattn_forward on HOST buffers: q, k, v are read from
+ * host memory and out is written to host memory, with the copies pipelined
+ * against the kernels.
+ *
+ * The heads (batch * n_heads) are cut into up to four chunks of whole heads.
+ * Three streams the library keeps per device carry, for each chunk, the
+ * host-to-device copies of its q, k and v, the two kernels of vattn_forward,
+ * and the device-to-host copy of its output, so that the copies of one chunk
+ * overlap the kernels of the next.  The result is bit-identical to
+ * vattn_forward on the same values (the same kernels per head).
+ *
+ * q, k, v, out: HOST pointers to contiguous f32 [batch, n_heads, n_patches,
+ *   head_dim], head-major, 4-byte aligned; out must not overlap q, k or v.
+ *   Page-locked memory (cudaHostAlloc / cudaHostRegister) lets the copies
+ *   run asynchronously and overlap; pageable memory gives the same result
+ *   with the copies serialised by the driver.
+ * stream: a cudaStream_t passed as void* (NULL = legacy default stream).  The
+ *   work is ordered after what was queued on `stream` and `stream` continues
+ *   only after the last copy out: out may be read once `stream` has been
+ *   synchronised.  The caller must keep all four buffers alive until then.
+ * Workspace (stream-ordered on `stream`, from the library's per-device pool):
+ *   two chunks of f32 inputs and outputs plus one chunk of f16 staging.
+ * Errors: those of vattn_forward; argument errors on the host before any
+ *   CUDA call.
+ */
+vattn_status vattn_forward_host(const float* q, const float* k, const float* v, float* out,
+                                int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, void* stream);
+
+/*
  * Size of the fixed staging scratch of vattn_forward_noalloc: 32 MiB, enough
  * for batch*n_heads*n_patches*round_up(head_dim, 16) <= 5,592,320 (for
  * example 16 heads x 4,100 patches at head_dim 72, or 64 heads x 1,024

@@ -20,7 +20,7 @@ def test_exports_every_declared_symbol(lib):
     names = _lib.exported_symbols()
     assert set(names) == {"vattn_forward", "vattn_forward_f16", "vattn_forward_f16io",
                           "vattn_forward_noalloc", "vattn_forward_accurate",
-                          "vattn_conv1d_step",
+                          "vattn_conv1d_step", "vattn_forward_host",
                           "vattn_rope_neox", "vattn_forward_rope",
                           "vattn_device_status", "vattn_status_string",
                           "vattn_last_error_string", "vattn_version"}
@@ -66,6 +66,9 @@ def test_host_side_argument_errors(lib, args, status):
     assert lib.vattn_last_error_string().decode() != ""
     # and so does the accurate (split-f16) one
     assert _lib.forward_accurate_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""
+    # and the host-buffer one
+    assert _lib.forward_host_status(*args, 0) == status
     assert lib.vattn_last_error_string().decode() != ""
 
 
@@ -123,6 +126,7 @@ def test_empty_problems_are_no_ops_even_with_null_pointers(lib, b, h, n):
     assert _lib.forward_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
     assert _lib.forward_noalloc_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
     assert _lib.forward_accurate_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
+    assert _lib.forward_host_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
 
 
 B4 = FAKE + 2 ** 24   # buffer

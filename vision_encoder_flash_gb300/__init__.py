@@ -10,7 +10,7 @@ missing or no GPU is present the calls raise.
 from __future__ import annotations
 
 from ._lib import (VattnError, _check, conv1d_step_status, device_status, exported_symbols,
-                   forward_accurate_status,
+                   forward_accurate_status, forward_host_status,
                    forward_f16_raw, forward_f16io_status,
                    forward_noalloc_raw, forward_raw, forward_rope_status, lib_path,
                    load_library, rope_neox_status, status_string, version)
@@ -27,9 +27,11 @@ def forward(q, k, v, out=None, stream=None):
     CUDA tensors: runs on their device and on ``stream`` (default: the
     current torch stream); returns ``out`` without synchronising.
 
-    CPU tensors: copies q, k, v to the current CUDA device, runs the kernel,
-    copies the result back into ``out`` (or a new pinned tensor) and
-    synchronises that stream before returning.
+    CPU tensors: one call of the host-buffer entry point (vattn_forward_host)
+    on the current CUDA device: chunks of heads are copied in, computed and
+    copied back into ``out`` (or a new pinned tensor) on overlapping
+    streams; the call synchronises ``stream`` before returning.  Pinned
+    (page-locked) inputs let the copies overlap the kernels.
     """
     import torch
 
@@ -46,17 +48,19 @@ def forward(q, k, v, out=None, stream=None):
         raise ValueError("q, k and v must be on the same device")
 
     if q.device.type == "cpu":
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous (head-major [B, H, N, D])")
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, pin_memory=True)
+        if (out.device.type != "cpu" or out.dtype != torch.float32 or out.shape != q.shape
+                or not out.is_contiguous()):
+            raise ValueError("out must be a contiguous float32 CPU tensor of q's shape")
         dev = torch.device("cuda", torch.cuda.current_device())
         s = stream if stream is not None else torch.cuda.current_stream(dev)
-        with torch.cuda.stream(s):
-            qd = q.to(dev, non_blocking=True)
-            kd = k.to(dev, non_blocking=True)
-            vd = v.to(dev, non_blocking=True)
-            od = torch.empty_like(qd)
-            _launch(qd, kd, vd, od, s)
-            if out is None:
-                out = torch.empty(q.shape, dtype=torch.float32, pin_memory=True)
-            out.copy_(od, non_blocking=True)
+        B, H, N, D = q.shape
+        _check(forward_host_status(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                                   N, D, s.cuda_stream))
         s.synchronize()
         return out
 

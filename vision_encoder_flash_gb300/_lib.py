@@ -51,6 +51,8 @@ def load_library():
     lib.vattn_forward_accurate.restype = ctypes.c_int
     lib.vattn_conv1d_step.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_conv1d_step.restype = ctypes.c_int
+    lib.vattn_forward_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.vattn_forward_host.restype = ctypes.c_int
     lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_noalloc.restype = ctypes.c_int
     lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -135,6 +137,14 @@ def conv1d_step_status(input_ptr, buffer_ptr, weight_ptr, output_ptr, batch, hid
     """vattn_conv1d_step with device addresses; returns the status code."""
     return int(load_library().vattn_conv1d_step(input_ptr, buffer_ptr, weight_ptr, output_ptr, batch,
                                                 hidden_size, kernel_size, d_conv, stream))
+
+
+def forward_host_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,
+                        stream=0) -> int:
+    """vattn_forward_host with HOST addresses (pipelined copies and kernels);
+    returns the status code.  The result is ready once `stream` is synchronised."""
+    return int(load_library().vattn_forward_host(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                                 n_patches, head_dim, stream))
 
 
 def forward_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int,

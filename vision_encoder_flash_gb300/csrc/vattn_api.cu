@@ -358,6 +358,72 @@ vattn_status launch_conv1d4(const vattn::Conv1dArgs& a, int device, int sms, cud
                           sms, stream);
 }
 
+// The two kernels of vattn_forward on device tensors of bh heads, with the
+// f16 workspace ws (three regions of `region` bytes) supplied by the caller.
+// Arguments are valid (checked by the entry points).
+vattn_status run_forward(const float* q, const float* k, const float* v, float* out, int64_t bh,
+                         int N, int D, void* ws, size_t region, cudaStream_t stream, int device) {
+  const int d_pad = (D + 15) & ~15;
+  const int nkb = d_pad <= 64 ? 1 : 2;
+  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+  vattn::Params p{};
+  p.out = out;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = d_pad;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  __half* q16 = static_cast<__half*>(ws);
+  __half* k16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + region);
+  __half* v16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + 2 * region);
+  CUtensorMap tq, tk, tv;
+  vattn_status st;
+  if ((st = make_tmap16(&tq, q16, bh, N, d_pad)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tk, k16, bh, N, d_pad)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tv, v16, bh, N, d_pad)) != VATTN_OK) return st;
+  const int64_t rows = bh * N;
+  const int vec = (D % 8 == 0) &&
+                  ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                    reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+  const long long chunks = 3LL * rows * (d_pad / 8);
+  const long long blocks = (chunks + 255) / 256;
+  const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
+  vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
+      vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, rows, D, d_pad, vec);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
+  const unsigned g = static_cast<unsigned>(grid);
+  if (nkb == 1 && nq == 2) return launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
+  if (nkb == 1) return launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
+  return launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+}
+
+// Three internal streams per device for the host-buffer entry point: host
+// to device copies, kernels, device to host copies.
+struct HostStreams {
+  std::once_flag once;
+  cudaStream_t s[3] = {nullptr, nullptr, nullptr};
+  cudaError_t err = cudaSuccess;
+};
+HostStreams g_host_streams[kMaxDevices];
+
+vattn_status host_streams(int device, cudaStream_t** out) {
+  if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
+  HostStreams& hs = g_host_streams[device];
+  std::call_once(hs.once, [&hs] {
+    for (int i = 0; i < 3 && hs.err == cudaSuccess; ++i)
+      hs.err = cudaStreamCreateWithFlags(&hs.s[i], cudaStreamNonBlocking);
+  });
+  if (hs.err != cudaSuccess) return cuda_fail(hs.err, "creating the copy and compute streams");
+  *out = hs.s;
+  return VATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -789,6 +855,133 @@ vattn_status vattn_conv1d_step(const float* input, float* buffer, const float* w
     case 7: return launch_conv1d4<7>(a, device, sms, stream);
     default: return launch_conv1d4<8>(a, device, sms, stream);
   }
+}
+
+vattn_status vattn_forward_host(const float* q, const float* k, const float* v, float* out,
+                                int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks: those of vattn_forward
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
+                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (head_dim > VATTN_MAX_HEAD_DIM)
+    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
+  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
+  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+
+  const int D = static_cast<int>(head_dim);
+  const int N = static_cast<int>(n_patches);
+  const int d_pad = (D + 15) & ~15;
+  // chunks of whole heads: up to four, so that copies in, kernels and copies
+  // out of consecutive chunks overlap
+  const int64_t hc = (bh + 3) / 4;                   // heads per chunk (the last may have fewer)
+  const int64_t n_chunks = (bh + hc - 1) / hc;        // 1..4, none empty
+  const uint64_t head_bytes = static_cast<uint64_t>(N) * D * 4u;
+  const auto round256 = [](uint64_t x) { return (x + 255u) & ~static_cast<uint64_t>(255u); };
+  const uint64_t in_slot = 3 * round256(hc * head_bytes);  // f32 q, k, v of one chunk
+  const uint64_t out_slot = round256(hc * head_bytes);
+  const uint64_t region = round256(static_cast<uint64_t>(hc) * N * d_pad * 2u);  // f16 staging
+  const uint64_t ws_bytes = 2 * in_slot + 2 * out_slot + 3 * region;
+
+  // ---- device side
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaStream_t* hs = nullptr;
+  vattn_status st = host_streams(device, &hs);
+  if (st != VATTN_OK) return st;
+  cudaMemPool_t pool = nullptr;
+  if ((st = pool_for(device, &pool)) != VATTN_OK) return st;
+  void* ws = nullptr;
+  e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  uint8_t* const base = static_cast<uint8_t*>(ws);
+  auto in_ptr = [&](int64_t c, int which) {
+    return reinterpret_cast<float*>(base + (c & 1) * in_slot + which * round256(hc * head_bytes));
+  };
+  auto out_ptr = [&](int64_t c) { return reinterpret_cast<float*>(base + 2 * in_slot + (c & 1) * out_slot); };
+  void* const ws16 = base + 2 * in_slot + 2 * out_slot;
+
+  // events: start, and per chunk copies in / kernels / copy out done
+  cudaEvent_t ev[1 + 3 * 4] = {};
+  int n_ev = 0;
+  for (; n_ev < 1 + 3 * n_chunks && st == VATTN_OK; ++n_ev) {
+    e = cudaEventCreateWithFlags(&ev[n_ev], cudaEventDisableTiming);
+    if (e != cudaSuccess) st = cuda_fail(e, "cudaEventCreate");
+  }
+  cudaEvent_t* ev_in = ev + 1;
+  cudaEvent_t* ev_comp = ev + 1 + n_chunks;
+  cudaEvent_t* ev_out = ev + 1 + 2 * n_chunks;
+  const cudaStream_t s_in = hs[0], s_comp = hs[1], s_out = hs[2];
+  auto ck = [&](cudaError_t err, const char* what) {
+    if (st == VATTN_OK && err != cudaSuccess) st = cuda_fail(err, what);
+    return st == VATTN_OK;
+  };
+  bool joined = false;
+  if (st == VATTN_OK && ck(cudaEventRecord(ev[0], stream), "cudaEventRecord") &&
+      ck(cudaStreamWaitEvent(s_in, ev[0], 0), "cudaStreamWaitEvent") &&
+      ck(cudaStreamWaitEvent(s_comp, ev[0], 0), "cudaStreamWaitEvent") &&
+      ck(cudaStreamWaitEvent(s_out, ev[0], 0), "cudaStreamWaitEvent")) {
+    for (int64_t c = 0; c < n_chunks && st == VATTN_OK; ++c) {
+      const int64_t h0 = c * hc;
+      const int64_t hn = (h0 + hc <= bh) ? hc : bh - h0;
+      const size_t nb = static_cast<size_t>(hn * head_bytes);
+      const size_t off = static_cast<size_t>(h0) * N * D;  // elements
+      // copies in; the slot is free once the kernels of chunk c - 2 ran
+      if (c >= 2 && !ck(cudaStreamWaitEvent(s_in, ev_comp[c - 2], 0), "cudaStreamWaitEvent")) break;
+      if (!ck(cudaMemcpyAsync(in_ptr(c, 0), q + off, nb, cudaMemcpyHostToDevice, s_in), "copy of q") ||
+          !ck(cudaMemcpyAsync(in_ptr(c, 1), k + off, nb, cudaMemcpyHostToDevice, s_in), "copy of k") ||
+          !ck(cudaMemcpyAsync(in_ptr(c, 2), v + off, nb, cudaMemcpyHostToDevice, s_in), "copy of v") ||
+          !ck(cudaEventRecord(ev_in[c], s_in), "cudaEventRecord"))
+        break;
+      // kernels; the output slot is free once the copy out of chunk c - 2 ran
+      if (!ck(cudaStreamWaitEvent(s_comp, ev_in[c], 0), "cudaStreamWaitEvent")) break;
+      if (c >= 2 && !ck(cudaStreamWaitEvent(s_comp, ev_out[c - 2], 0), "cudaStreamWaitEvent")) break;
+      st = run_forward(in_ptr(c, 0), in_ptr(c, 1), in_ptr(c, 2), out_ptr(c), hn, N, D, ws16,
+                       static_cast<size_t>(region), s_comp, device);
+      if (st != VATTN_OK || !ck(cudaEventRecord(ev_comp[c], s_comp), "cudaEventRecord")) break;
+      // copy out
+      if (!ck(cudaStreamWaitEvent(s_out, ev_comp[c], 0), "cudaStreamWaitEvent") ||
+          !ck(cudaMemcpyAsync(out + off, out_ptr(c), nb, cudaMemcpyDeviceToHost, s_out), "copy of out") ||
+          !ck(cudaEventRecord(ev_out[c], s_out), "cudaEventRecord"))
+        break;
+    }
+    // the caller's stream continues after the last copy out (which follows
+    // every kernel and copy of the call); on an error, after whatever was queued
+    if (st == VATTN_OK) {
+      joined = ck(cudaStreamWaitEvent(stream, ev_out[n_chunks - 1], 0), "cudaStreamWaitEvent");
+    }
+  }
+  if (!joined) {
+    // make the caller's stream (and so the release below) wait for all three streams
+    for (int i = 0; i < 3; ++i) {
+      cudaEvent_t tail = nullptr;
+      if (cudaEventCreateWithFlags(&tail, cudaEventDisableTiming) == cudaSuccess) {
+        if (cudaEventRecord(tail, hs[i]) == cudaSuccess) cudaStreamWaitEvent(stream, tail, 0);
+        cudaEventDestroy(tail);
+      }
+    }
+  }
+  for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);  // released once complete
+  e = cudaFreeAsync(ws, stream);
+  if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
+  return st;
 }
 
 vattn_status vattn_device_status(uint32_t* code) {
