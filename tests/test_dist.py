@@ -48,3 +48,10 @@ def test_single_process_helpers():
     import bench
     assert bench.max_over_ranks(1.5) == 1.5
     assert bench.weak_scaling_value(1e12, 1, 1000.0) == pytest.approx(1.0)
+
+
+def test_percentiles_nearest_rank():
+    import bench
+    assert bench.percentiles(list(range(1, 11))) == [1, 5, 9]
+    assert bench.percentiles([3.0]) == [3.0, 3.0, 3.0]
+    assert bench.percentiles([5, 1, 4, 2, 3], qs=(0, 100)) == [1, 5]
