@@ -305,6 +305,19 @@ vattn_status vattn_forward_noalloc(const float* q, const float* k, const float* 
  */
 vattn_status vattn_device_status(uint32_t* code);
 
+/*
+ * vattn_selftest_wait_timeout -- exercises the kernels' failure detection
+ * without faulting anything: launches on `stream` a one-thread kernel whose
+ * bounded wait, the same as every wait in the attention kernel, is on an
+ * mbarrier phase that nothing completes.  After the wait limit (about 2 s)
+ * it records a timeout with site code 15 in the status word and returns;
+ * the device stays usable.  vattn_device_status() then returns
+ * VATTN_ERR_DEVICE_TIMEOUT with *code == 0x10F and clears the word.  The
+ * shader has no counterpart: this exists to test the timeout path.
+ * Returns VATTN_OK once launched, or VATTN_ERR_CUDA.
+ */
+vattn_status vattn_selftest_wait_timeout(void* stream);
+
 /* Static text for a status code. */
 const char* vattn_status_string(vattn_status status);
 

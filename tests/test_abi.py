@@ -21,6 +21,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == {"vattn_forward", "vattn_forward_f16", "vattn_forward_f16io",
                           "vattn_forward_noalloc", "vattn_forward_accurate",
                           "vattn_conv1d_step", "vattn_forward_host",
+                          "vattn_selftest_wait_timeout",
                           "vattn_rope_neox", "vattn_forward_rope",
                           "vattn_device_status", "vattn_status_string",
                           "vattn_last_error_string", "vattn_version"}

@@ -55,6 +55,8 @@ def load_library():
     lib.vattn_forward_host.restype = ctypes.c_int
     lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_noalloc.restype = ctypes.c_int
+    lib.vattn_selftest_wait_timeout.argtypes = [vp]
+    lib.vattn_selftest_wait_timeout.restype = ctypes.c_int
     lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.vattn_device_status.restype = ctypes.c_int
     lib.vattn_status_string.argtypes = [ctypes.c_int]
@@ -161,6 +163,11 @@ def forward_noalloc_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patch
     """Like forward_noalloc_raw but returns the status code instead of raising."""
     return int(load_library().vattn_forward_noalloc(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                                     n_patches, head_dim, stream))
+
+
+def selftest_wait_timeout(stream: int = 0) -> None:
+    """Launch the self-test kernel whose bounded wait runs out (about 2 s)."""
+    _check(load_library().vattn_selftest_wait_timeout(stream))
 
 
 def device_status() -> int:

@@ -424,6 +424,28 @@ vattn_status host_streams(int device, cudaStream_t** out) {
   return VATTN_OK;
 }
 
+// Wait site reported by the self-test of the timeout path.
+constexpr uint32_t kSiteSelfTest = 15;
+
+// One thread waits, with the kernels' bounded wait, for phase 0 of an
+// mbarrier that nothing arrives on: after the wait limit it records a
+// timeout in the status word, exactly as a stalled attention kernel would,
+// and returns.
+__global__ void vattn_selftest_wait_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    vattn::ptx::mbar_init(vattn::ptx::smem_addr(&bar), 1);
+    abort_flag = 0;
+    vattn::ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const vattn::Waiter w{&abort_flag};
+    w.wait(vattn::ptx::smem_addr(&bar), 0u, kSiteSelfTest);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -982,6 +1004,14 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
   e = cudaFreeAsync(ws, stream);
   if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
   return st;
+}
+
+vattn_status vattn_selftest_wait_timeout(void* stream_ptr) {
+  g_last_error[0] = '\0';
+  vattn_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream_ptr)>>>();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test kernel launch");
+  return VATTN_OK;
 }
 
 vattn_status vattn_device_status(uint32_t* code) {
