@@ -84,24 +84,13 @@ def test_f16_entry_matches_oracle_and_f32_entry(torch_dev, shape):
     assert np.array_equal(got, same), f"{shape}: f16 entry differs from the f32 entry"
 
 
-@pytest.mark.parametrize("idx", [3, 4])
+@pytest.mark.parametrize("idx", [3, 4, 5])
 def test_f16_entry_on_workloads(torch_dev, idx):
+    # every output element against the oracle on the f16 values
     q, k, v = workload_inputs(idx)
     q16, k16, v16 = to_f16(q), to_f16(k), to_f16(v)
     got = run_f16(torch_dev, q16, k16, v16)
-    b, h, n, _ = q.shape
-    rng = np.random.default_rng(31 + idx)
-    rows = np.concatenate([rng.integers(0, b * h * n, 256), [0, b * h * n - 1]])
-    assert_against_oracle(got, q16, k16, v16, rows=rows, what=f"workload {idx}")
-
-
-def test_f16_entry_on_the_largest_workload_sampled(torch_dev):
-    q, k, v = workload_inputs(5)
-    q16, k16, v16 = to_f16(q), to_f16(k), to_f16(v)
-    got = run_f16(torch_dev, q16, k16, v16)
-    b, h, n, _ = q.shape
-    rows = np.random.default_rng(5).integers(0, b * h * n, 192)
-    assert_against_oracle(got, q16, k16, v16, rows=rows, what="workload 5")
+    assert_against_oracle(got, q16, k16, v16, what=f"workload {idx}")
 
 
 def test_f16_entry_on_a_side_stream(torch_dev):
@@ -155,14 +144,13 @@ def test_f16io_is_the_f16_entry_rounded_to_f16(torch_dev, shape, out_offset):
     assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), f"{shape}: differs"
 
 
-def test_f16io_on_the_largest_workload_sampled(torch_dev):
+def test_f16io_on_the_largest_workload(torch_dev):
     q, k, v = workload_inputs(5)
     q16, k16, v16 = to_f16(q), to_f16(k), to_f16(v)
     got = run_f16io(torch_dev, q16, k16, v16).astype(np.float32)
-    b, h, n, d = q.shape
-    rows = np.random.default_rng(55).integers(0, b * h * n, 192)
-    ref = oracle.rows(*(x.astype(np.float32) for x in (q16, k16, v16)), rows)
-    diff = got.reshape(-1, d)[rows].astype(np.float64) - ref
+    n = q.shape[2]
+    ref = oracle.forward(*(x.astype(np.float32) for x in (q16, k16, v16)))
+    diff = got.astype(np.float64) - ref
     # f16 output rounding (2^-11 relative) on top of the kernel-arithmetic bound
     bound = (2.0 ** -10 + n * 2.0 ** -24) * float(np.abs(v16.astype(np.float32)).max()) + 1e-5
     assert float(np.abs(diff).max()) <= bound

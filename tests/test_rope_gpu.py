@@ -167,8 +167,4 @@ def test_fused_rope_on_workloads(torch_dev, idx):
     d = q.shape[-1]
     got = run_fused(torch_dev, q, k, v, d, 0, 10000.0)
     qr, kr = fused_reference(q, k, v, d, 0, 10000.0)
-    b, h, n, _ = q.shape
-    rng = np.random.default_rng(77 + idx)
-    rows = np.concatenate([rng.integers(0, b * h * n, 512), [0, b * h * n - 1]])
-    ref = oracle.rows(qr, kr, v, rows)
-    assert_close(got.reshape(-1, d)[rows], ref, f"workload {idx}", MAX_REL_L2)
+    assert_close(got, oracle.forward(qr, kr, v), f"workload {idx}", MAX_REL_L2)
