@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
       if (lane == 0) {
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
+        ptx::grid_dep_wait();  // the previous kernel (the staging pass) has written K and V
         if constexpr (kAcc) {
           ptx::prefetch_tensormap(&tm_kl);
           ptx::prefetch_tensormap(&tm_vl);
@@ -337,6 +338,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
       if (lane == 0) {
         ptx::prefetch_tensormap(&tm_q);
         if constexpr (kAcc) ptx::prefetch_tensormap(&tm_ql);
+        ptx::grid_dep_wait();  // ... and Q
         int q_issued = 0;
         for (int i = 0; i < n_mine; ++i) {
           if (i > 0 && !w.wait(bar(kBarQEmpty), static_cast<uint32_t>(i - 1) & 1u, kSiteProducerQ))

@@ -287,6 +287,13 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, boo
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// ------------------------------------------------- programmatic launches
+// Waits until the grids this one depends on have completed and their memory
+// operations are visible (a no-op without a programmatic dependency).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the dependent grid launch once every block of this grid has run it.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

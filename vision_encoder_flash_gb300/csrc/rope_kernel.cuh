@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(256) vattn_stage_rope_kernel(StageJob a, Stage
     h.w = ptx::pack_half2(x[6], x[7]);
     *reinterpret_cast<uint4*>(job.dst + row * d_pad + ch * 8) = h;
   }
+  ptx::grid_dep_launch();  // the attention kernel may launch once every block got here
 }
 
 }  // namespace vattn

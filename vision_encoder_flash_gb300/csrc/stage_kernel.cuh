@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(256) vattn_stage_kernel(StageJob a, StageJob b
     h.w = ptx::pack_half2(x[6], x[7]);
     *reinterpret_cast<uint4*>(job.dst + row * d_pad + ch * 8) = h;
   }
+  ptx::grid_dep_launch();  // the attention kernel may launch once every block got here
 }
 
 }  // namespace vattn
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(256) vattn_stage_split_kernel(SplitJob a, Spli
     *reinterpret_cast<uint4*>(job.dst + row * d_pad + ch * 8) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(job.dst_lo + row * d_pad + ch * 8) = make_uint4(l[0], l[1], l[2], l[3]);
   }
+  ptx::grid_dep_launch();  // the attention kernel may launch once every block got here
 }
 
 }  // namespace vattn

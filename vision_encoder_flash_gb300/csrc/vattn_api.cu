@@ -195,8 +195,21 @@ vattn_status launch_attention_maps(const CUtensorMap& tq, const CUtensorMap& tk,
     if (so != VATTN_OK) return so;
     p.tma_out = 1;
   }
-  kernel<<<grid, P::kThreads, P::kSmemBytes, stream>>>(tq, tk, tv, to, tql, tkl, tvl, p);
-  const cudaError_t e = cudaGetLastError();
+  // programmatic launch: the block prologue (barriers, TMEM, tensor maps)
+  // overlaps the end of the previous kernel; the producers wait for it
+  // (griddepcontrol.wait) before their first load
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(P::kThreads);
+  cfg.dynamicSmemBytes = P::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, tql, tkl, tvl, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   return VATTN_OK;
 }
