@@ -525,7 +525,7 @@ def run_vattn(args, workload):
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "vision_encoder_flash_gb300.forward on pinned host tensors (vattn_forward_host: four chunks of heads, copies overlapping the kernels)"},
+                "path": "vision_encoder_flash_gb300.forward on pinned host tensors (vattn_forward_host: eight chunks of heads, copies overlapping the kernels)"},
         "gpu_launches": 2 * args.steps,  # staging kernel + attention kernel per step
         "other_workloads": extras,
         "variants": variants,

@@ -228,7 +228,7 @@ vattn_status vattn_conv1d_step(const float* input, float* buffer, const float* w
  * host memory and out is written to host memory, with the copies pipelined
  * against the kernels.
  *
- * The heads (batch * n_heads) are cut into up to four chunks of whole heads.
+ * The heads (batch * n_heads) are cut into up to eight chunks of whole heads.
  * Three streams the library keeps per device carry, for each chunk, the
  * host-to-device copies of its q, k and v, the two kernels of vattn_forward,
  * and the device-to-host copy of its output, so that the copies of one chunk

@@ -1,6 +1,6 @@
 """GPU tests of the host-buffer entry point (vattn_forward_host), through the
 C ABI: q, k, v in host memory, out written to host memory, heads cut into up
-to four chunks whose copies and kernels overlap.  The kernels per head are
+to eight chunks whose copies and kernels overlap.  The kernels per head are
 those of vattn_forward, so the result must be bit-identical to it; and it is
 checked against the f64 oracle with the acceptance bar (max abs 3e-3, rel L2
 1e-3; twice the rel-L2 bar off the seeded workloads, as elsewhere)."""
@@ -51,9 +51,10 @@ def host_forward(torch_dev, q, k, v, pinned=True, stream=None):
     return out.numpy()
 
 
-# batch*n_heads 1..7: one chunk, chunks of one head, ragged last chunks
+# batch*n_heads 1..17: one chunk, chunks of one head, chunks of two and
+# three heads with a smaller last chunk (10 = 5 x 2; 17 = 5 x 3 + 2)
 SHAPES = [(1, 1, 200, 64), (1, 3, 129, 72), (2, 3, 300, 40), (1, 5, 77, 17), (7, 1, 256, 128),
-          (1, 4, 1, 8)]
+          (1, 4, 1, 8), (2, 5, 130, 64), (1, 17, 64, 32)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)

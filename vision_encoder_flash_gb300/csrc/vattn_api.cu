@@ -416,6 +416,11 @@ vattn_status run_forward(const float* q, const float* k, const float* v, float* 
   return launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
 }
 
+// Most chunks of heads a host-buffer call is cut into (measured on the
+// 8x16x2304x64 workload: 4 chunks 1.37 ms, 8 chunks 1.34 ms, 16 chunks
+// 1.43 ms per call).
+constexpr int64_t kHostChunks = 8;
+
 // Three internal streams per device for the host-buffer entry point: host
 // to device copies, kernels, device to host copies.
 struct HostStreams {
@@ -922,10 +927,10 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
   const int D = static_cast<int>(head_dim);
   const int N = static_cast<int>(n_patches);
   const int d_pad = (D + 15) & ~15;
-  // chunks of whole heads: up to four, so that copies in, kernels and copies
-  // out of consecutive chunks overlap
-  const int64_t hc = (bh + 3) / 4;                   // heads per chunk (the last may have fewer)
-  const int64_t n_chunks = (bh + hc - 1) / hc;        // 1..4, none empty
+  // chunks of whole heads, so that copies in, kernels and copies out of
+  // consecutive chunks overlap
+  const int64_t hc = (bh + kHostChunks - 1) / kHostChunks;  // heads per chunk (the last may have fewer)
+  const int64_t n_chunks = (bh + hc - 1) / hc;               // 1..kHostChunks, none empty
   const uint64_t head_bytes = static_cast<uint64_t>(N) * D * 4u;
   const auto round256 = [](uint64_t x) { return (x + 255u) & ~static_cast<uint64_t>(255u); };
   const uint64_t in_slot = 3 * round256(hc * head_bytes);  // f32 q, k, v of one chunk
@@ -954,7 +959,7 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
   void* const ws16 = base + 2 * in_slot + 2 * out_slot;
 
   // events: start, and per chunk copies in / kernels / copy out done
-  cudaEvent_t ev[1 + 3 * 4] = {};
+  cudaEvent_t ev[1 + 3 * kHostChunks] = {};
   int n_ev = 0;
   for (; n_ev < 1 + 3 * n_chunks && st == VATTN_OK; ++n_ev) {
     e = cudaEventCreateWithFlags(&ev[n_ev], cudaEventDisableTiming);
