@@ -96,7 +96,11 @@ struct Plan {
   static constexpr int kParts = kAcc ? 2 : 1;      // f16 terms per operand
   static constexpr int kPartBytes = kTileF16;      // offset of lo after hi
   static constexpr int kStageStride = kParts * kTileF16;
-  static constexpr int kStages = kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : 3);  // K and V stages
+  static constexpr int kStages =  // K and V stages
+      kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3));
+  // two query tiles with head_dim > 64: O needs 2 x 80..128 TMEM columns, so
+  // the two tiles take turns with one P buffer
+  static constexpr bool kSharedP = NQ == 2 && NKB == 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + NQ * kStageStride;
   static constexpr int kOffV = kOffK + kStages * kStageStride;
@@ -112,15 +116,19 @@ struct Plan {
   static constexpr bool kSplitRegs = NQ == 2;
   static constexpr uint32_t kRegsSoftmax = 224;
   static constexpr uint32_t kRegsOther = 56;
-  // TMEM columns (kAcc: P hi at 256, P lo at 320, O at 384)
+  // TMEM columns: S buffers at 0 and 128, P at 256 (kAcc: P lo at 320), O
+  // after them; two query tiles keep their P (and O) blocks kColPStride
+  // (kColOStride) apart.  Shared P (two query tiles, head_dim > 64): one P
+  // block at 256 and O blocks at 320 and 416, so d_pad <= 96.
   static constexpr uint32_t kColP = 256;
   static constexpr uint32_t kColPlo = 320;
-  static constexpr uint32_t kColO = (NQ == 2 || kAcc) ? 384 : 320;
-  static constexpr uint32_t kColStride = 64;  // between the tiles' P (and O) blocks
+  static constexpr uint32_t kColO = kSharedP ? 320 : ((NQ == 2 || kAcc) ? 384 : 320);
+  static constexpr uint32_t kColPStride = kSharedP ? 0 : 64;
+  static constexpr uint32_t kColOStride = kSharedP ? 96 : 64;
   static_assert(!kSplitRegs || kRegsOther + NQ * kRegsSoftmax <= (1 + NQ) * 168,
                 "register split too large");
   static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
-  static_assert(NQ == 1 || NKB == 1, "two query tiles need head_dim <= 64");
+  static_assert(!kSharedP || !kAcc, "shared P is for the f16 path");
   static_assert(!kAcc || NQ == 1, "the accurate mode takes one query tile");
 };
 
@@ -261,7 +269,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(kBarSFull + i), 1);
       ptx::mbar_init(bar(kBarSFree + i), NQ == 2 ? 8 : 4);
-      ptx::mbar_init(bar(kBarPFull + i), 4 * NQ);
+      ptx::mbar_init(bar(kBarPFull + i), P::kSharedP ? 4 : 4 * NQ);
       ptx::mbar_init(bar(kBarODone + i), 1);
     }
     ptx::mbar_init(bar(kBarMmaDone), 2);
@@ -412,8 +420,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
         const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
         auto issue_pv = [&](int t, int64_t g, bool first) {
           const uint32_t vb = base_s + P::kOffV + kv_stage(g) * P::kStageStride;
-          const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
-          const uint32_t a = tmem + P::kColP + static_cast<uint32_t>(t) * P::kColStride;
+          const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColOStride;
+          const uint32_t a = tmem + P::kColP + static_cast<uint32_t>(t) * P::kColPStride;
           for (int ks = 0; ks < kBN / 16; ++ks) {
             ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
                         ptx::smem_desc(vb + ks * 2048, kBoxBytes, 1024, ptx::kSwizzle128B),
@@ -437,9 +445,19 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
             if (!(ok = w.wait(bar(kBarVFull + kv_stage(g)), kv_phase(g), kSiteMmaV))) break;
             // P of key tile g written (for the first key tile of a tile this
             // also tells that the softmax has read the previous tile's O)
-            if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
-            ptx::tc_fence_after();
-            for (int t = 0; t < NQ; ++t) issue_pv(t, g, j == 0);
+            if constexpr (P::kSharedP) {
+              // the two query tiles take turns with the P buffer
+              for (int t = 0; ok && t < NQ; ++t) {
+                if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
+                ptx::tc_fence_after();
+                issue_pv(t, g, j == 0);
+              }
+              if (!ok) break;
+            } else {
+              if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
+              ptx::tc_fence_after();
+              for (int t = 0; t < NQ; ++t) issue_pv(t, g, j == 0);
+            }
             ptx::mma_commit(bar(kBarVEmpty + kv_stage(g)));
           }
         }
@@ -452,8 +470,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t p_addr = tmem + lane_addr + P::kColP + static_cast<uint32_t>(t) * P::kColStride;
-    const uint32_t o_addr = tmem + lane_addr + P::kColO + static_cast<uint32_t>(t) * P::kColStride;
+    const uint32_t p_addr = tmem + lane_addr + P::kColP + static_cast<uint32_t>(t) * P::kColPStride;
+    const uint32_t o_addr = tmem + lane_addr + P::kColO + static_cast<uint32_t>(t) * P::kColOStride;
     bool ok = true;
     for (int i = 0; ok && i < n_mine; ++i) {
       float m_ref = -INFINITY;  // running max in log2 units (may lag the true max by < 8)
@@ -526,13 +544,27 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
         const float2 s01 = __fadd2_rn(acc[0], acc[1]);
         const float2 s23 = __fadd2_rn(acc[2], acc[3]);
         l = fmaf(l, alpha, (s01.x + s01.y) + (s23.x + s23.y));
-        if (j > 0) {
+        if (P::kSharedP) {
+          // one P buffer, used by (tile 0, g), (tile 1, g), (tile 0, g + 1), ...:
+          // tile 0 waits for the P V of (1, g - 1), tile 1 for that of (0, g).
+          // One thread issues them in that order, so either also means the
+          // tile's own previous P V has finished (O final for a rescale).
+          const int64_t gw = t == 0 ? g - 1 : g;
+          if (gw >= 0) {
+            if (!(ok = w.wait_warp(bar(kBarODone + (1 - t)), static_cast<uint32_t>(gw & 1),
+                                   kSiteSoftO)))
+              break;
+            ptx::tc_fence_after();
+          }
+        } else if (j > 0) {
           // P V of the previous key tile has finished: P buffer free, O final.
           // (For j == 0 the previous tile's epilogue already waited for it.)
           if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>((g - 1) & 1),
                                  kSiteSoftO)))
             break;
           ptx::tc_fence_after();
+        }
+        if (j > 0) {
           if (__any_sync(0xffffffffu, need)) {
             for (int c = 0; c < (p.d_pad >> 4); ++c) {
               uint32_t y[16];
@@ -554,7 +586,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
 
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        warp_arrive(bar(kBarPFull));
+        warp_arrive(bar(kBarPFull + (P::kSharedP ? t : 0)));
       }
       if (!ok) break;
       // ---- epilogue of the tile: out = O / l for the rows < n_patches.  The

@@ -222,6 +222,25 @@ vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, cons
                                                        stream, device);
 }
 
+// Query tiles per work tile: two when there is more than one tile of rows
+// and the TMEM plan holds two O blocks (d_pad <= 64 with separate P buffers,
+// d_pad <= 96 with a shared one), else one.
+int query_tiles(int n_patches, int d_pad) {
+  return (n_patches > vattn::kBM && d_pad <= 96) ? 2 : 1;
+}
+
+// The kernel variant for nkb 64-column blocks of d_pad and nq query tiles.
+template <bool kOut16 = false>
+vattn_status dispatch_attention(int nkb, int nq, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, vattn::Params p, unsigned g,
+                                cudaStream_t stream, int device) {
+  if (nkb == 1)
+    return nq == 2 ? launch_attention<2, 1, kOut16>(tq, tk, tv, p, g, stream, device)
+                   : launch_attention<1, 1, kOut16>(tq, tk, tv, p, g, stream, device);
+  return nq == 2 ? launch_attention<2, 2, kOut16>(tq, tk, tv, p, g, stream, device)
+                 : launch_attention<1, 2, kOut16>(tq, tk, tv, p, g, stream, device);
+}
+
 // Arguments of the NeoX rotation (checked on the host, before any CUDA call).
 vattn_status check_rope(int64_t head_dim, int64_t n_patches, int64_t rope_dims, int64_t pos0,
                         float base, const float* factors) {
@@ -292,7 +311,7 @@ vattn_status forward_f16_impl(const uint16_t* q, const uint16_t* k, const uint16
   const int N = static_cast<int>(n_patches);
   const int d_pad = (D + 15) & ~15;
   const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int nq = query_tiles(N, d_pad);
   const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
   const int64_t grid = bh * n_qblocks;
   if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
@@ -321,9 +340,7 @@ vattn_status forward_f16_impl(const uint16_t* q, const uint16_t* k, const uint16
   if ((st = make_tmap16(&tv, reinterpret_cast<const __half*>(v), bh, N, D)) != VATTN_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const unsigned g = static_cast<unsigned>(grid);
-  if (nkb == 1 && nq == 2) return launch_attention<2, 1, kOut16>(tq, tk, tv, p, g, stream, device);
-  if (nkb == 1) return launch_attention<1, 1, kOut16>(tq, tk, tv, p, g, stream, device);
-  return launch_attention<1, 2, kOut16>(tq, tk, tv, p, g, stream, device);
+  return dispatch_attention<kOut16>(nkb, nq, tq, tk, tv, p, g, stream, device);
 }
 
 // Blocks of `threads` threads of `kernel` that fit on one multiprocessor,
@@ -378,7 +395,7 @@ vattn_status run_forward(const float* q, const float* k, const float* v, float* 
                          int N, int D, void* ws, size_t region, cudaStream_t stream, int device) {
   const int d_pad = (D + 15) & ~15;
   const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int nq = query_tiles(N, d_pad);
   const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
   const int64_t grid = bh * n_qblocks;
   if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
@@ -411,9 +428,7 @@ vattn_status run_forward(const float* q, const float* k, const float* v, float* 
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
   const unsigned g = static_cast<unsigned>(grid);
-  if (nkb == 1 && nq == 2) return launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
-  if (nkb == 1) return launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
-  return launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+  return dispatch_attention(nkb, nq, tq, tk, tv, p, g, stream, device);
 }
 
 // Most chunks of heads a host-buffer call is cut into (measured on the
@@ -499,7 +514,7 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   const int N = static_cast<int>(n_patches);
   const int d_pad = (D + 15) & ~15;
   const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int nq = query_tiles(N, d_pad);
   const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
   const int64_t grid = bh * n_qblocks;
   if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
@@ -551,12 +566,7 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
       st = cuda_fail(e, "staging kernel launch");
     } else {
       const unsigned g = static_cast<unsigned>(grid);
-      if (nkb == 1 && nq == 2)
-        st = launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
-      else if (nkb == 1)
-        st = launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
-      else
-        st = launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+      st = dispatch_attention(nkb, nq, tq, tk, tv, p, g, stream, device);
     }
   }
   // back to the pool once the launches above have run (stream order)
@@ -673,7 +683,7 @@ vattn_status vattn_forward_rope(const float* q, const float* k, const float* v, 
   const int d_pad = (D + 15) & ~15;
   const int half = static_cast<int>(rope_dims / 2);
   const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int nq = query_tiles(N, d_pad);
   const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
   const int64_t grid = bh * n_qblocks;
   if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
@@ -731,12 +741,7 @@ vattn_status vattn_forward_rope(const float* q, const float* k, const float* v, 
     }
     if (st == VATTN_OK) {
       const unsigned g = static_cast<unsigned>(grid);
-      if (nkb == 1 && nq == 2)
-        st = launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
-      else if (nkb == 1)
-        st = launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
-      else
-        st = launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+      st = dispatch_attention(nkb, nq, tq, tk, tv, p, g, stream, device);
     }
   }
   e = cudaFreeAsync(ws, stream);
@@ -1154,7 +1159,7 @@ extern "C" vattn_status vattn_forward_noalloc(const float* q, const float* k, co
                 "(VATTN_NOALLOC_MAX_SCRATCH_BYTES): call vattn_forward instead",
                 (unsigned long long)(3u * region), (unsigned long long)kNoAllocScratchBytes);
   const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = (nkb == 1 && N > vattn::kBM) ? 2 : 1;
+  const int nq = query_tiles(N, d_pad);
   const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
   const int64_t grid = bh * n_qblocks;
   if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
@@ -1202,7 +1207,5 @@ extern "C" vattn_status vattn_forward_noalloc(const float* q, const float* k, co
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
   const unsigned g = static_cast<unsigned>(grid);
-  if (nkb == 1 && nq == 2) return launch_attention<2, 1>(tq, tk, tv, p, g, stream, device);
-  if (nkb == 1) return launch_attention<1, 1>(tq, tk, tv, p, g, stream, device);
-  return launch_attention<1, 2>(tq, tk, tv, p, g, stream, device);
+  return dispatch_attention(nkb, nq, tq, tk, tv, p, g, stream, device);
 }
