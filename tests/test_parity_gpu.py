@@ -103,6 +103,19 @@ def test_small_shapes(torch_dev, d, n):
 PAIR = [(d, n) for d in (8, 20, 32, 48, 60, 64) for n in (257, 511, 512, 513, 1025)]
 
 
+# head_dim 65..96 with more than one query tile: two query tiles that share
+# one P buffer, two column blocks, several work tiles per head, ragged ends
+SHARED_P = [(d, n) for d in (65, 70, 88, 96) for n in (129, 257, 511, 1025)]
+
+
+@pytest.mark.parametrize("d,n", SHARED_P)
+def test_shared_p_shapes(torch_dev, d, n):
+    q, k, v = make_inputs(1, 3, n, d, seed=3500 + 11 * d + n)
+    got = run_gpu(torch_dev, q, k, v)
+    assert_kernel_arithmetic(got, q, k, v, what=f"shared P D={d} N={n}")
+    assert_parity(got, oracle.forward(q, k, v), f"shared P D={d} N={n}", rel_l2=2 * MAX_REL_L2)
+
+
 @pytest.mark.parametrize("d,n", PAIR)
 def test_pair_shapes(torch_dev, d, n):
     q, k, v = make_inputs(1, 3, n, d, seed=3000 + 11 * d + n)
