@@ -28,10 +28,15 @@
 //     row, so the row max and row sum need no shuffles; exp is exp2 with
 //     log2(e) folded into one FMA; O is rescaled in TMEM only when the
 //     row max grew by more than 2^8 (exact after the final 1/l);
-//   * the same warpgroup divides by l and stores its rows of out (f32).
+//   * the same warpgroup divides by l and stores its rows of out (f32);
+//   * the producers wait for the previous kernel (griddepcontrol.wait)
+//     before their first load, so with a programmatic launch the block
+//     prologue overlaps the end of the staging pass.
 // TMEM columns (512): S buffers [0,128) and [128,256); with two query tiles
-// P0, P1 at 256, 320 and O0, O1 at 384, 448 (head_dim <= 64); with one query
-// tile P at 256 and O at 320 (head_dim <= 128).
+// P0, P1 at 256, 320 and O0, O1 at 384, 448 (head_dim <= 64), or one P
+// buffer at 256 that the two tiles take in turn and O0, O1 at 320, 416
+// (head_dim 65..96); with one query tile P at 256 and O at 320 (head_dim
+// <= 128; the accurate mode: P hi 256, P lo 320, O 384).
 // Every wait is bounded: on timeout the block records the wait site in
 // g_vattn_status, raises a shared abort flag so the other roles leave their
 // loops, drains its own TMA copies and MMAs, frees TMEM and exits.
