@@ -269,6 +269,47 @@ bool overlaps2(const void* a, uint64_t a_bytes, const void* b, uint64_t b_bytes)
   return x < y + b_bytes && y < x + a_bytes;
 }
 
+// Size rules of the f32 attention entry points, checked before any CUDA call.
+vattn_status check_attention_sizes(int64_t batch, int64_t n_heads, int64_t n_patches,
+                                   int64_t head_dim) {
+  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
+    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
+                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
+  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
+  if (head_dim > VATTN_MAX_HEAD_DIM)
+    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  return VATTN_OK;
+}
+
+// Tensor rules of the f32 attention entry points (sizes already checked):
+// *bh receives batch * n_heads; *empty is set, and nothing more checked,
+// when there is nothing to compute.
+vattn_status check_attention_tensors(const float* q, const float* k, const float* v,
+                                     const float* out, int64_t batch, int64_t n_heads,
+                                     int64_t n_patches, int64_t head_dim, int64_t* bh,
+                                     bool* empty) {
+  *empty = false;
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  *bh = batch * n_heads;
+  if (*bh == 0 || n_patches == 0) {
+    *empty = true;
+    return VATTN_OK;
+  }
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || *bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / *bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t bytes = static_cast<uint64_t>(*bh) * n_patches * head_dim * 4u;
+  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
+  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+  return VATTN_OK;
+}
+
 // The attention kernel alone on f16 inputs; out is f32 (kOut16 == false) or
 // f16 (kOut16 == true).
 template <bool kOut16>
@@ -277,12 +318,8 @@ vattn_status forward_f16_impl(const uint16_t* q, const uint16_t* k, const uint16
                               int64_t head_dim, void* stream_ptr) {
   g_last_error[0] = '\0';
   // ---- host-side checks, before any CUDA call
-  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
-    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
-                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
-  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
-  if (head_dim > VATTN_MAX_HEAD_DIM)
-    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
+  const vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
   if (head_dim % 8 != 0)
     return fail(VATTN_ERR_UNSUPPORTED,
                 "f16 inputs need head_dim %% 8 == 0 (16-byte rows), got %lld: use vattn_forward",
@@ -488,27 +525,13 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
                            void* stream_ptr) {
   g_last_error[0] = '\0';
   // ---- host-side checks, before any CUDA call
-  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
-    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
-                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
-  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
-  if (head_dim > VATTN_MAX_HEAD_DIM)
-    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
-  if (batch != 0 && n_heads > INT64_MAX / batch)
-    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
-  const int64_t bh = batch * n_heads;
-  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
-  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
-  if (n_patches > INT32_MAX || bh > INT32_MAX)
-    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
-  if (n_patches > INT64_MAX / head_dim / bh / 4)
-    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
-  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
-  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
-  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
-  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
-    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+  vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  int64_t bh = 0;
+  bool empty = false;
+  chk = check_attention_tensors(q, k, v, out, batch, n_heads, n_patches, head_dim, &bh, &empty);
+  if (chk != VATTN_OK) return chk;
+  if (empty) return VATTN_OK;  // nothing to compute
 
   const int D = static_cast<int>(head_dim);
   const int N = static_cast<int>(n_patches);
@@ -654,29 +677,15 @@ vattn_status vattn_forward_rope(const float* q, const float* k, const float* v, 
                                 const float* factors, void* stream_ptr) {
   g_last_error[0] = '\0';
   // ---- host-side checks (those of vattn_forward and of the rotation)
-  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
-    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
-                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
-  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
-  if (head_dim > VATTN_MAX_HEAD_DIM)
-    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
-  vattn_status st = check_rope(head_dim, n_patches, rope_dims, pos0, base, factors);
-  if (st != VATTN_OK) return st;
-  if (batch != 0 && n_heads > INT64_MAX / batch)
-    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
-  const int64_t bh = batch * n_heads;
-  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
-  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
-  if (n_patches > INT32_MAX || bh > INT32_MAX)
-    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
-  if (n_patches > INT64_MAX / head_dim / bh / 4)
-    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
-  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
-  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
-  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
-  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
-    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+  vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  chk = check_rope(head_dim, n_patches, rope_dims, pos0, base, factors);
+  if (chk != VATTN_OK) return chk;
+  int64_t bh = 0;
+  bool empty = false;
+  chk = check_attention_tensors(q, k, v, out, batch, n_heads, n_patches, head_dim, &bh, &empty);
+  if (chk != VATTN_OK) return chk;
+  if (empty) return VATTN_OK;  // nothing to compute
 
   const int D = static_cast<int>(head_dim);
   const int N = static_cast<int>(n_patches);
@@ -706,7 +715,8 @@ vattn_status vattn_forward_rope(const float* q, const float* k, const float* v, 
   const size_t region = (static_cast<size_t>(rows) * d_pad * 2 + 255) & ~static_cast<size_t>(255);
   const size_t tab_bytes = static_cast<size_t>(N) * (half > 0 ? half : 1) * sizeof(float2);
   cudaMemPool_t pool = nullptr;
-  if ((st = pool_for(device, &pool)) != VATTN_OK) return st;
+  vattn_status st = pool_for(device, &pool);
+  if (st != VATTN_OK) return st;
   void* ws = nullptr;
   e = cudaMallocFromPoolAsync(&ws, 3 * region + tab_bytes, pool, stream);
   if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
@@ -754,27 +764,13 @@ vattn_status vattn_forward_accurate(const float* q, const float* k, const float*
                                     int64_t head_dim, void* stream_ptr) {
   g_last_error[0] = '\0';
   // ---- host-side checks: those of vattn_forward
-  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
-    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
-                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
-  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
-  if (head_dim > VATTN_MAX_HEAD_DIM)
-    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
-  if (batch != 0 && n_heads > INT64_MAX / batch)
-    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
-  const int64_t bh = batch * n_heads;
-  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
-  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
-  if (n_patches > INT32_MAX || bh > INT32_MAX)
-    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
-  if (n_patches > INT64_MAX / head_dim / bh / 4)
-    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
-  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
-  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
-  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
-  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
-    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+  vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  int64_t bh = 0;
+  bool empty = false;
+  chk = check_attention_tensors(q, k, v, out, batch, n_heads, n_patches, head_dim, &bh, &empty);
+  if (chk != VATTN_OK) return chk;
+  if (empty) return VATTN_OK;  // nothing to compute
 
   const int D = static_cast<int>(head_dim);
   const int N = static_cast<int>(n_patches);
@@ -907,27 +903,13 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
                                 int64_t head_dim, void* stream_ptr) {
   g_last_error[0] = '\0';
   // ---- host-side checks: those of vattn_forward
-  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
-    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
-                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
-  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
-  if (head_dim > VATTN_MAX_HEAD_DIM)
-    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
-  if (batch != 0 && n_heads > INT64_MAX / batch)
-    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
-  const int64_t bh = batch * n_heads;
-  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
-  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
-  if (n_patches > INT32_MAX || bh > INT32_MAX)
-    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
-  if (n_patches > INT64_MAX / head_dim / bh / 4)
-    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
-  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
-  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
-  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
-  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
-    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+  vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  int64_t bh = 0;
+  bool empty = false;
+  chk = check_attention_tensors(q, k, v, out, batch, n_heads, n_patches, head_dim, &bh, &empty);
+  if (chk != VATTN_OK) return chk;
+  if (empty) return VATTN_OK;  // nothing to compute
 
   const int D = static_cast<int>(head_dim);
   const int N = static_cast<int>(n_patches);
@@ -1124,27 +1106,13 @@ extern "C" vattn_status vattn_forward_noalloc(const float* q, const float* k, co
   g_last_error[0] = '\0';
   // ---- host-side checks (the rules of vattn_forward plus the scratch size),
   //      before any CUDA call
-  if (batch < 0 || n_heads < 0 || n_patches < 0 || head_dim < 0)
-    return fail(VATTN_ERR_INVALID_ARG, "negative size (batch=%lld n_heads=%lld n_patches=%lld head_dim=%lld)",
-                (long long)batch, (long long)n_heads, (long long)n_patches, (long long)head_dim);
-  if (head_dim == 0) return fail(VATTN_ERR_INVALID_ARG, "head_dim must be >= 1");
-  if (head_dim > VATTN_MAX_HEAD_DIM)
-    return fail(VATTN_ERR_UNSUPPORTED, "head_dim %lld > %d", (long long)head_dim, VATTN_MAX_HEAD_DIM);
-  if (batch != 0 && n_heads > INT64_MAX / batch)
-    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
-  const int64_t bh = batch * n_heads;
-  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
-  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
-  if (n_patches > INT32_MAX || bh > INT32_MAX)
-    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
-  if (n_patches > INT64_MAX / head_dim / bh / 4)
-    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
-  const uint64_t bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
-  const uintptr_t align_or = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                             reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
-  if (align_or & 3u) return fail(VATTN_ERR_MISALIGNED, "tensor pointers must be 4-byte aligned");
-  if (overlaps(out, q, bytes) || overlaps(out, k, bytes) || overlaps(out, v, bytes))
-    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+  vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  int64_t bh = 0;
+  bool empty = false;
+  chk = check_attention_tensors(q, k, v, out, batch, n_heads, n_patches, head_dim, &bh, &empty);
+  if (chk != VATTN_OK) return chk;
+  if (empty) return VATTN_OK;  // nothing to compute
 
   const int D = static_cast<int>(head_dim);
   const int N = static_cast<int>(n_patches);
