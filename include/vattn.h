@@ -54,14 +54,20 @@ typedef enum {
  * head_dim: 1..128.  Any n_patches >= 0 (ragged tails are handled).
  * stream: a cudaStream_t passed as void* (NULL = legacy default stream).
  *
- * The call is asynchronous: it validates arguments, launches two kernels on
- * `stream` (the f16 staging of q, k and v, then the attention kernel) and
- * returns; the result is ready when the stream reaches that point.  The
- * f16 copies (3 * batch*n_heads*n_patches*round_up(head_dim, 16) * 2 bytes)
- * live in a workspace taken stream-ordered from a memory pool the library
- * keeps per device (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`;
- * the pool keeps its memory between calls).  batch*n_heads == 0 or
- * n_patches == 0 is a successful no-op that launches nothing.
+ * The call is asynchronous: it validates arguments, launches its kernels on
+ * `stream` and returns; the result is ready when the stream reaches that
+ * point.  Two paths, the same f16 rounding and bit-identical results:
+ *   - 128 < n_patches <= 2048, head_dim 33..64 and a multiple of 4, q, k, v
+ *     16-byte aligned: one kernel that reads the f32 tiles and rounds them
+ *     to f16 in shared memory; nothing is allocated;
+ *   - otherwise two kernels (the f16 staging of q, k and v, then the
+ *     attention kernel).  The f16 copies (3 * batch*n_heads*n_patches*
+ *     round_up(head_dim, 16) * 2 bytes) live in a workspace taken
+ *     stream-ordered from a memory pool the library keeps per device
+ *     (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`; the pool keeps
+ *     its memory between calls).
+ * batch*n_heads == 0 or n_patches == 0 is a successful no-op that launches
+ * nothing.
  *
  * Returns VATTN_OK, or an error code with no kernel launched (argument
  * errors are detected on the host, before any CUDA call), or VATTN_ERR_CUDA

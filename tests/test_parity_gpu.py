@@ -248,3 +248,66 @@ def test_host_tensors_round_trip(torch_dev):
     out = vef.forward(pin(q), pin(k), pin(v))
     assert out.device.type == "cpu"
     assert_parity(out.numpy(), oracle.forward(q, k, v), "host tensors")
+
+
+# The direct f32 path (one kernel that rounds q, k, v to f16 in shared
+# memory): 128 < n_patches <= 2048, head_dim 33..64 and a multiple of 4,
+# 16-byte aligned inputs.  Ragged ends, the 2048 limit, and enough heads that
+# every block takes several work tiles (40 heads x 4 query blocks > 152).
+DIRECT = [(1, 3, n, d) for d in (36, 44, 52, 64) for n in (129, 255, 256, 257, 1000, 2048)]
+DIRECT += [(2, 40, 1000, 64), (1, 160, 300, 40)]
+
+
+def run_gpu_offset(torch_dev, q, k, v, offset_elems):
+    """vattn_forward with every tensor starting offset_elems f32 past a
+    fresh allocation (offset 1: 4-byte aligned only, which takes the
+    two-kernel path)."""
+    torch, dev = torch_dev
+    numel = q.size
+    ts = []
+    for x in (q, k, v):
+        t = torch.zeros(numel + 4, device=dev)
+        t[offset_elems:offset_elems + numel] = torch.from_numpy(x.ravel()).to(dev)
+        ts.append(t)
+    out = torch.zeros(numel + 4, device=dev)
+    vef.forward_raw(ts[0].data_ptr() + 4 * offset_elems, ts[1].data_ptr() + 4 * offset_elems,
+                    ts[2].data_ptr() + 4 * offset_elems, out.data_ptr() + 4 * offset_elems,
+                    *q.shape, torch.cuda.current_stream(dev).cuda_stream)
+    torch.cuda.synchronize(dev)
+    assert vef.device_status() == 0
+    return out[offset_elems:offset_elems + numel].cpu().numpy().reshape(q.shape)
+
+
+@pytest.mark.parametrize("shape", DIRECT)
+def test_direct_f32_path(torch_dev, shape):
+    q, k, v = make_inputs(*shape, seed=5000 + 13 * shape[3] + shape[2] + shape[1])
+    got = run_gpu(torch_dev, q, k, v)
+    b, h, n, d = shape
+    # sampled rows (flat (b*H + h)*N + i) plus the first and last of every head
+    rng = np.random.default_rng(n + h)
+    heads = np.arange(b * h) * n
+    rows = np.union1d(rng.choice(b * h * n, size=min(b * h * n, 256), replace=False),
+                      np.concatenate([heads, heads + n - 1]))
+    sel = got.reshape(-1, d)[rows]
+    assert_kernel_arithmetic(sel, q, k, v, rows=rows, what=f"direct {shape}")
+    assert_parity(sel, oracle.rows(q, k, v, rows), f"direct {shape}", rel_l2=2 * MAX_REL_L2)
+
+
+@pytest.mark.parametrize("shape", [(1, 3, 1000, 64), (2, 40, 1000, 64), (1, 2, 2048, 48),
+                                   (1, 2, 129, 36)])
+def test_direct_and_staged_paths_agree_bitwise(torch_dev, shape):
+    # the same rounding (f32 -> f16, nearest even) and the same attention
+    # kernel arithmetic on both paths: identical bits
+    q, k, v = make_inputs(*shape, seed=5100 + shape[2])
+    direct = run_gpu_offset(torch_dev, q, k, v, 4)   # 16-byte aligned: one kernel
+    staged = run_gpu_offset(torch_dev, q, k, v, 1)   # 4-byte aligned: staging + attention
+    assert np.array_equal(direct.view(np.uint32), staged.view(np.uint32))
+
+
+@pytest.mark.parametrize("n", [2048, 2049])
+def test_direct_path_limit(torch_dev, n):
+    # 2048 patches take the single kernel, 2049 the two passes: both correct
+    q, k, v = make_inputs(1, 1, n, 64, seed=5200 + n)
+    got = run_gpu(torch_dev, q, k, v)
+    rows = np.array([0, 1, 1023, n - 2, n - 1])  # one head: flat index = row
+    assert_parity(got.reshape(-1, 64)[rows], oracle.rows(q, k, v, rows), f"limit N={n}")

@@ -7,7 +7,12 @@
 // f32 online softmax with running (m, l, o), no 1/sqrt(head_dim) factor.
 //
 // Inputs are the f16 copies written by vattn_stage_kernel (stage_kernel.cuh):
-// [B*H, N, d_pad] f16, d_pad = head_dim rounded up to 16, zero padding.
+// [B*H, N, d_pad] f16, d_pad = head_dim rounded up to 16, zero padding --
+// or, in the kF32 variant (two query tiles, head_dim <= 64), the caller's f32
+// tensors: TMA brings f32 tiles into a ring of shared-memory slots and a
+// fourth warpgroup rounds them to f16 into the same swizzled operand tiles,
+// with the staging kernel's rounding (round to nearest even), so both paths
+// give bit-identical results.
 // The shader's design (8 queries x 32 keys per 64-thread workgroup, scalar
 // dot products, subgroup reductions) is replaced by a GB300 one:
 //   * a work tile = one bh and NQ query tiles of 128 rows; the grid is one
@@ -72,6 +77,7 @@ enum WaitSite : uint32_t {
   kSiteDrainTma = 12,
   kSiteDrainMma = 13,
   kSiteMmaSFree = 14,
+  kSiteConvert = 16,
 };
 constexpr uint32_t kStatusTimeout = 0x100u;
 
@@ -94,15 +100,19 @@ struct Params {
 // f16 tiles: NKB blocks of [128 rows x 128 bytes], 128-byte swizzle.
 // kAcc (accurate mode, one query tile): every Q, K and V tile comes as an
 // f16 pair (hi, lo), the lo part right after the hi part.
-template <int NQ, int NKB, bool kAcc = false>
+// kF32 (f32 inputs, two query tiles, head_dim <= 64): q, k and v tiles come
+// in as f32 [128 rows x 64 columns] into a ring of two slots, and a fourth
+// warpgroup rounds them to f16 into the same swizzled tiles.
+template <int NQ, int NKB, bool kAcc = false, bool kF32 = false>
 struct Plan {
-  static constexpr int kThreads = 128 * (1 + NQ);  // control warpgroup + softmax
+  // control warpgroup + one softmax warpgroup per query tile (+ converters)
+  static constexpr int kThreads = 128 * (1 + NQ) + (kF32 ? 128 : 0);
   static constexpr int kTileF16 = NKB * kBoxBytes;
   static constexpr int kParts = kAcc ? 2 : 1;      // f16 terms per operand
   static constexpr int kPartBytes = kTileF16;      // offset of lo after hi
   static constexpr int kStageStride = kParts * kTileF16;
   static constexpr int kStages =  // K and V stages
-      kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3));
+      kF32 ? 2 : (kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3)));
   // two query tiles with head_dim > 64: O needs 2 x 80..128 TMEM columns, so
   // the two tiles take turns with one P buffer
   static constexpr bool kSharedP = NQ == 2 && NKB == 2;
@@ -113,14 +123,20 @@ struct Plan {
   // 2 KB buffers (32 rows x 16 f32, 64-byte swizzle) per softmax warp
   static constexpr int kEpiBytes = (NKB == 1 && !kAcc) ? 4 * NQ * 4096 : 0;
   static constexpr int kOffEpi = kOffV + kStages * kStageStride;
-  static constexpr int kOffBar = kOffEpi + kEpiBytes;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kF32Slots = kF32 ? 3 : 0;
+  static constexpr int kF32TileBytes = kBM * 64 * 4;  // 128 rows x 64 f32, unswizzled
+  static constexpr int kOffF32 = kOffEpi + kEpiBytes;
+  static constexpr int kOffBar = kOffF32 + kF32Slots * kF32TileBytes;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   // register split (two query tiles): control warpgroup 56, softmax 224;
   // launch gives 65536 / 384 -> 168 per thread, 56 + 2 * 224 <= 3 * 168.
+  // With the converter warpgroup: 65536 / 512 -> 128 per thread,
+  // 2 * 40 + 2 * 216 <= 4 * 128.
   static constexpr bool kSplitRegs = NQ == 2;
-  static constexpr uint32_t kRegsSoftmax = 224;
-  static constexpr uint32_t kRegsOther = 56;
+  static constexpr uint32_t kRegsSoftmax = kF32 ? 216 : 224;
+  static constexpr uint32_t kRegsOther = kF32 ? 40 : 56;
+  static constexpr uint32_t kRegsLaunch = kF32 ? 128 : 168;
   // TMEM columns: S buffers at 0 and 128, P at 256 (kAcc: P lo at 320), O
   // after them; two query tiles keep their P (and O) blocks kColPStride
   // (kColOStride) apart.  Shared P (two query tiles, head_dim > 64): one P
@@ -130,8 +146,11 @@ struct Plan {
   static constexpr uint32_t kColO = kSharedP ? 320 : ((NQ == 2 || kAcc) ? 384 : 320);
   static constexpr uint32_t kColPStride = kSharedP ? 0 : 64;
   static constexpr uint32_t kColOStride = kSharedP ? 96 : 64;
-  static_assert(!kSplitRegs || kRegsOther + NQ * kRegsSoftmax <= (1 + NQ) * 168,
+  static_assert(!kSplitRegs || (kF32 ? 2 : 1) * kRegsOther + NQ * kRegsSoftmax <=
+                                    static_cast<uint32_t>(kThreads / 128) * kRegsLaunch,
                 "register split too large");
+  static_assert(!kF32 || (NQ == 2 && NKB == 1 && !kAcc), "f32 inputs: two query tiles, head_dim <= 64");
+  static_assert(kF32Slots <= 4, "f32 ring barriers");
   static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
   static_assert(!kSharedP || !kAcc, "shared P is for the f16 path");
   static_assert(!kAcc || NQ == 1, "the accurate mode takes one query tile");
@@ -139,10 +158,10 @@ struct Plan {
 
 // mbarrier indices inside the barrier block (kStages <= 5).
 enum Bar : int {
-  kBarQFull = 0,      // Q tiles landed                     (1 + tx)
-  kBarKFull = 1,      // [5] K stage landed                 (1 + tx)
+  kBarQFull = 0,      // Q tiles landed                     (1 + tx; f32 inputs: 4 per tile)
+  kBarKFull = 1,      // [5] K stage landed                 (1 + tx; f32 inputs: 4)
   kBarKEmpty = 6,     // [5] S MMAs done with K stage       (commit)
-  kBarVFull = 11,     // [5] V stage landed                 (1 + tx)
+  kBarVFull = 11,     // [5] V stage landed                 (1 + tx; f32 inputs: 4)
   kBarVEmpty = 16,    // [5] P.V MMAs done with V stage     (commit)
   kBarSFull = 21,     // [2] S buffer complete in TMEM      (commit)
   kBarSFree = 23,     // [2] S buffer(s) copied to registers (one per softmax warp;
@@ -151,11 +170,13 @@ enum Bar : int {
   kBarODone = 27,     // [2] P.V of query tile complete     (commit)
   kBarMmaDone = 29,   // every MMA of the block complete    (one commit per issuer)
   kBarQEmpty = 30,    // S products of a tile done with its Q tiles (commit)
-  kNumBars = 31,
+  kBarF32Full = 31,   // [4] f32 ring slot landed           (1 + tx)
+  kBarF32Empty = 35,  // [4] f32 ring slot read (one per converter warp)
+  kNumBars = 39,
 };
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
 constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
-static_assert(kAbortOff + 4 <= 256, "barrier block overflow");
+static_assert(kAbortOff + 4 <= 512, "barrier block overflow");
 
 struct Waiter {
   volatile uint32_t* abort_flag;
@@ -216,8 +237,13 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
 // into P hi and P lo, and each product takes three MMAs:
 //   S = Qh Kh^T + Qh Kl^T + Ql Kh^T,   O += Ph Vh + Ph Vl + Pl Vh
 // (the lo x lo terms are below 2^-22 relative).
-template <int NQ, int NKB, bool kOut16 = false, bool kAcc = false>
-__global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
+// kF32: tm_q / tm_k / tm_v are f32 [B*H, N, head_dim] maps with boxes of
+// {64 columns, 128 rows}, no swizzle (head_dim % 4 == 0, <= 64); warp 0
+// streams the tiles (per work tile: K_0, V_0, Q_0, Q_1, K_1, V_1, ...) into
+// a two-slot f32 ring, and warps 12..15 round each one to f16 into its
+// swizzled Q, K or V tile (the f16 staging pass is not needed).
+template <int NQ, int NKB, bool kOut16 = false, bool kAcc = false, bool kF32 = false>
+__global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
     vattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
@@ -225,7 +251,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_ql,
                      const __grid_constant__ CUtensorMap tm_kl,
                      const __grid_constant__ CUtensorMap tm_vl, const Params p) {
-  using P = Plan<NQ, NKB, kAcc>;
+  using P = Plan<NQ, NKB, kAcc, kF32>;
   constexpr int S = P::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = ptx::smem_addr(smem_raw);
@@ -263,13 +289,18 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
   auto kv_phase = [](int64_t g) -> uint32_t { return static_cast<uint32_t>((g / S) & 1); };
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(bar(kBarQFull), 1);
+    // f32 inputs: the converter warps (four) arrive on the f16 tiles' barriers
+    ptx::mbar_init(bar(kBarQFull), kF32 ? 4 * NQ : 1);
     ptx::mbar_init(bar(kBarQEmpty), 1);
     for (int i = 0; i < S; ++i) {
-      ptx::mbar_init(bar(kBarKFull + i), 1);
+      ptx::mbar_init(bar(kBarKFull + i), kF32 ? 4 : 1);
       ptx::mbar_init(bar(kBarKEmpty + i), 1);
-      ptx::mbar_init(bar(kBarVFull + i), 1);
+      ptx::mbar_init(bar(kBarVFull + i), kF32 ? 4 : 1);
       ptx::mbar_init(bar(kBarVEmpty + i), 1);
+    }
+    for (int i = 0; i < P::kF32Slots; ++i) {
+      ptx::mbar_init(bar(kBarF32Full + i), 1);
+      ptx::mbar_init(bar(kBarF32Empty + i), 4);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(kBarSFull + i), 1);
@@ -291,10 +322,100 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + P::kOffBar + kTmemSlotOff);
   const uint32_t tile_bytes = static_cast<uint32_t>(P::kTileF16);
 
-  const bool softmax_wg = warp >= 4;
-  if (!softmax_wg) {
+  const bool softmax_wg = warp >= 4 && warp < 4 + 4 * NQ;
+  const bool convert_wg = kF32 && warp >= 4 + 4 * NQ;
+  if (convert_wg) {
     if (P::kSplitRegs) ptx::regs_decrease<P::kRegsOther>();
-    if (warp == 0) {
+    // ------------------------------------------------ f32 -> f16 converters
+    // Ring tile n (slot n % 2) is the n-th of the sequence warp 0 loads; it
+    // goes to the K or V stage of its key tile or to a Q tile once the MMAs
+    // are done with that buffer.  Warp cw rounds rows [32 cw, 32 cw + 32):
+    // per step two rows, 16 lanes per row, four f32 columns per lane, into
+    // the 128-byte-swizzled f16 layout TMA would have written (16-byte unit
+    // u of row r at u ^ (r & 7)).
+    const int cw = warp - (4 + 4 * NQ);
+    int64_t n = 0;
+    auto convert = [&](uint32_t dst, int full_bar) -> bool {
+      const int slot = static_cast<int>(n % P::kF32Slots);
+      if (!w.wait_warp(bar(kBarF32Full + slot), static_cast<uint32_t>((n / P::kF32Slots) & 1),
+                       kSiteConvert))
+        return false;
+      const uint32_t src = base_s + P::kOffF32 + static_cast<uint32_t>(slot * P::kF32TileBytes);
+      const int c4 = lane & 15;  // f32 columns 4 c4 .. 4 c4 + 3
+#pragma unroll 4
+      for (int it = 0; it < 16; ++it) {
+        const int r = 32 * cw + 2 * it + (lane >> 4);
+        const float4 x = ptx::ld_shared_v4(src + static_cast<uint32_t>(r * 256 + c4 * 16));
+        const uint32_t unit = static_cast<uint32_t>((c4 >> 1) ^ (r & 7));
+        ptx::st_shared_v2(dst + static_cast<uint32_t>(r * 128) + unit * 16u +
+                              static_cast<uint32_t>(c4 & 1) * 8u,
+                          ptx::pack_half2(x.x, x.y), ptx::pack_half2(x.z, x.w));
+      }
+      ptx::fence_proxy_async_smem();  // the tensor core reads what was written
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(bar(kBarF32Empty + slot));
+        ptx::mbar_arrive(bar(full_bar));
+      }
+      ++n;
+      return true;
+    };
+    bool ok = true;
+    for (int i = 0; ok && i < n_mine; ++i) {
+      for (int j = 0; ok && j < T; ++j) {
+        const int64_t g = static_cast<int64_t>(i) * T + j;
+        const int st = kv_stage(g);
+        const uint32_t free_par = kv_phase(g) ^ 1u;
+        if (!(ok = w.wait_warp(bar(kBarKEmpty + st), free_par, kSiteConvert))) break;
+        if (!(ok = convert(base_s + P::kOffK + st * P::kStageStride, kBarKFull + st))) break;
+        if (!(ok = w.wait_warp(bar(kBarVEmpty + st), free_par, kSiteConvert))) break;
+        if (!(ok = convert(base_s + P::kOffV + st * P::kStageStride, kBarVFull + st))) break;
+        if (j == 0) {
+          // the Q tiles of tile i, once the S products of tile i - 1 are done
+          if (i > 0 && !(ok = w.wait_warp(bar(kBarQEmpty), static_cast<uint32_t>(i - 1) & 1u,
+                                          kSiteConvert)))
+            break;
+          for (int t = 0; ok && t < NQ; ++t)
+            ok = convert(base_s + P::kOffQ + t * P::kStageStride, kBarQFull);
+        }
+      }
+    }
+  } else if (!softmax_wg) {
+    if (P::kSplitRegs) ptx::regs_decrease<P::kRegsOther>();
+    if (kF32 && warp == 0) {
+      // -------------------------------------------------- f32 ring producer
+      if (lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        ptx::grid_dep_wait();  // the previous kernel's writes of q, k, v are visible
+        int64_t n = 0;
+        auto load = [&](const CUtensorMap* tm, int row0, int bh) -> bool {
+          const int slot = static_cast<int>(n % P::kF32Slots);
+          if (!w.wait(bar(kBarF32Empty + slot),
+                      static_cast<uint32_t>(((n / P::kF32Slots) & 1) ^ 1), kSiteProducerK))
+            return false;
+          ptx::mbar_arrive_expect_tx(bar(kBarF32Full + slot), P::kF32TileBytes);
+          ptx::tma_load_3d(base_s + P::kOffF32 + static_cast<uint32_t>(slot * P::kF32TileBytes),
+                           tm, bar(kBarF32Full + slot), 0, row0, bh);
+          ++n;
+          return true;
+        };
+        bool ok = true;
+        for (int i = 0; ok && i < n_mine; ++i) {
+          const int bh = tile_bh(i);
+          for (int j = 0; ok && j < T; ++j) {
+            ok = load(&tm_k, j * kBN, bh) && load(&tm_v, j * kBN, bh);
+            for (int t = 0; ok && j == 0 && t < NQ; ++t)
+              ok = load(&tm_q, tile_row0(i) + t * kBM, bh);
+          }
+        }
+        // every issued copy must have landed before the block exits
+        for (int64_t m = (n > P::kF32Slots ? n - P::kF32Slots : 0); m < n; ++m)
+          w.drain(bar(kBarF32Full + static_cast<int>(m % P::kF32Slots)),
+                  static_cast<uint32_t>((m / P::kF32Slots) & 1), kSiteDrainTma);
+      }
+    } else if (warp == 0) {
       // ------------------------------------------------- K/V producer
       // Runs ahead across tile boundaries: the next tile's first K/V tiles
       // are in flight while the current one ends.
@@ -344,7 +465,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc>::kThreads, 1)
         for (int64_t g = (v_issued > S ? v_issued - S : 0); g < v_issued; ++g)
           w.drain(bar(kBarVFull + kv_stage(g)), kv_phase(g), kSiteDrainTma);
       }
-    } else if (warp == 3) {
+    } else if (warp == 3 && !kF32) {
       // --------------------------------------------------- Q producer
       // The Q tiles of tile i go in as soon as the S products of tile i-1
       // have read the previous ones.

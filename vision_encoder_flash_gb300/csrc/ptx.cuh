@@ -88,6 +88,19 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, fl
                : "memory");
 }
 
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 // 3-D tiled bulk tensor store shared -> global (bulk-group completion).
 // Elements of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t c0,

@@ -92,6 +92,29 @@ vattn_status make_tmap16(CUtensorMap* tm, const __half* ptr, int64_t bh, int64_t
 // swizzle) or f16 (32 bytes, 32-byte swizzle): the layouts the kernel writes
 // to its staging buffers.  Needs rows of whole 16-byte units (head_dim % 4 ==
 // 0 for f32, % 8 == 0 for f16) and a 16-byte aligned base.
+// f32 [bh, n, d] (d % 4 == 0, 16-byte aligned base) with boxes of {64
+// columns, 128 rows}, no swizzle; columns past d and rows past n read as zero.
+vattn_status make_tmap32(CUtensorMap* tm, const float* ptr, int64_t bh, int64_t n, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    if (g_encode_err != cudaSuccess) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
+    return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                              static_cast<cuuint64_t>(bh)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4u,
+                                 static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(d) * 4u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(vattn::kBM), 1u};
+  const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims,
+                         strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(VATTN_ERR_CUDA, "cuTensorMapEncodeTiled (f32) failed with CUresult %d", static_cast<int>(r));
+  return VATTN_OK;
+}
+
 vattn_status make_tmap_out(CUtensorMap* tm, void* out, int64_t bh, int64_t n, int d, bool f16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
@@ -164,14 +187,14 @@ vattn_status sm_count(int device, int* out) {
 // one per tile), each looping over the tiles blockIdx.x + k * gridDim.x.
 // tql, tkl, tvl: the lo halves of q, k, v (accurate mode only; otherwise
 // unused and any valid map may be passed).
-template <int NQ, int NKB, bool kOut16, bool kAcc>
+template <int NQ, int NKB, bool kOut16, bool kAcc, bool kF32 = false>
 vattn_status launch_attention_maps(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const CUtensorMap& tql,
                                    const CUtensorMap& tkl, const CUtensorMap& tvl,
                                    vattn::Params p, unsigned n_tiles, cudaStream_t stream,
                                    int device) {
-  using P = vattn::Plan<NQ, NKB, kAcc>;
-  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kOut16, kAcc>;
+  using P = vattn::Plan<NQ, NKB, kAcc, kF32>;
+  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kOut16, kAcc, kF32>;
   static std::atomic<uint8_t> configured[kMaxDevices];
   if (!configured[device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -227,6 +250,46 @@ vattn_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, cons
 // d_pad <= 96 with a shared one), else one.
 int query_tiles(int n_patches, int d_pad) {
   return (n_patches > vattn::kBM && d_pad <= 96) ? 2 : 1;
+}
+
+// f32 inputs the attention kernel reads directly (its converter warps round
+// them to f16 in shared memory, no staging pass): two query tiles, head_dim
+// 33..64 and a multiple of 4, 16-byte aligned q, k, v, and n_patches <= 2048.
+// Each block rounds the K and V tiles of its own query rows, so a head's
+// keys are rounded once per 256 query rows and the shared-memory traffic
+// grows with n_patches; measured on GB300 (8 x 16 heads, head_dim 64) the
+// single kernel is 1.65x faster than staging + attention at 256 patches,
+// 1.23x at 1024, even at 2048 and 0.98x at 2304.  Narrower heads stage
+// cheaper (head_dim 32 at 1024 patches: 0.96x), so they keep the two passes.
+bool f32_direct(const float* q, const float* k, const float* v, int N, int D) {
+  const int d_pad = (D + 15) & ~15;
+  return d_pad <= 64 && D > 32 && D % 4 == 0 && N <= 2048 && query_tiles(N, d_pad) == 2 &&
+         ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+           reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+}
+
+// The attention kernel on f32 inputs (f32_direct(...) holds): one launch.
+vattn_status launch_f32_direct(const float* q, const float* k, const float* v, float* out,
+                               int64_t bh, int N, int D, cudaStream_t stream, int device) {
+  const int64_t n_qblocks = (N + 2 * vattn::kBM - 1) / (2 * vattn::kBM);
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+  vattn::Params p{};
+  p.out = out;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = (D + 15) & ~15;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  CUtensorMap tq, tk, tv;
+  vattn_status st;
+  if ((st = make_tmap32(&tq, q, bh, N, D)) != VATTN_OK) return st;
+  if ((st = make_tmap32(&tk, k, bh, N, D)) != VATTN_OK) return st;
+  if ((st = make_tmap32(&tv, v, bh, N, D)) != VATTN_OK) return st;
+  return launch_attention_maps<2, 1, false, false, true>(tq, tk, tv, tq, tk, tv, p,
+                                                         static_cast<unsigned>(grid), stream, device);
 }
 
 // The kernel variant for nkb 64-column blocks of d_pad and nq query tiles.
@@ -430,6 +493,7 @@ vattn_status launch_conv1d4(const vattn::Conv1dArgs& a, int device, int sms, cud
 // Arguments are valid (checked by the entry points).
 vattn_status run_forward(const float* q, const float* k, const float* v, float* out, int64_t bh,
                          int N, int D, void* ws, size_t region, cudaStream_t stream, int device) {
+  if (f32_direct(q, k, v, N, D)) return launch_f32_direct(q, k, v, out, bh, N, D, stream, device);
   const int d_pad = (D + 15) & ~15;
   const int nkb = d_pad <= 64 ? 1 : 2;
   const int nq = query_tiles(N, d_pad);
@@ -557,6 +621,7 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (f32_direct(q, k, v, N, D)) return launch_f32_direct(q, k, v, out, bh, N, D, stream, device);
 
   // f16 copies of q, k, v ([B*H, N, d_pad] each), stream-ordered workspace
   const int64_t rows = bh * N;
