@@ -61,11 +61,13 @@ typedef enum {
  *     16-byte aligned: one kernel that reads the f32 tiles and rounds them
  *     to f16 in shared memory; nothing is allocated;
  *   - otherwise two kernels (the f16 staging of q, k and v, then the
- *     attention kernel).  The f16 copies (3 * batch*n_heads*n_patches*
- *     round_up(head_dim, 16) * 2 bytes) live in a workspace taken
- *     stream-ordered from a memory pool the library keeps per device
- *     (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`; the pool keeps
- *     its memory between calls).
+ *     attention kernel; with head_dim <= 64 and a multiple of 4, more than
+ *     128 patches and q 16-byte aligned, the attention kernel rounds q
+ *     itself and the staging kernel only k and v).  The f16 copies
+ *     (at most 3 * batch*n_heads*n_patches*round_up(head_dim, 16) * 2
+ *     bytes) live in a workspace taken stream-ordered from a memory pool the
+ *     library keeps per device (cudaMallocFromPoolAsync / cudaFreeAsync on
+ *     `stream`; the pool keeps its memory between calls).
  * batch*n_heads == 0 or n_patches == 0 is a successful no-op that launches
  * nothing.
  *
@@ -122,6 +124,29 @@ vattn_status vattn_forward_f16(const uint16_t* q, const uint16_t* k, const uint1
 vattn_status vattn_forward_f16io(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  uint16_t* out, int64_t batch, int64_t n_heads,
                                  int64_t n_patches, int64_t head_dim, void* stream);
+
+/*
+ * vattn_forward_f32q -- attention with f32 queries and f16 keys and values.
+ *
+ * For callers that hold k and v in f16 (computed once, attended by fresh
+ * f32 queries).  It is also the attention kernel that vattn_forward runs
+ * after its staging pass when 2048 < n_patches and head_dim <= 64: the
+ * kernel rounds q to f16 itself (round to nearest even) once per block of
+ * query rows, so the result equals vattn_forward on q and the f32 values of
+ * k and v, bit for bit.
+ *
+ * q, out: DEVICE f32 [batch, n_heads, n_patches, head_dim]; k, v: DEVICE
+ *   IEEE binary16 tensors of the same shape.  q, k, v 16-byte aligned, out
+ *   4-byte aligned, out not overlapping q, k or v.
+ * Shapes: head_dim a multiple of 8 and at most 64, n_patches > 128 (the
+ *   kernel variant with two 128-row query tiles per block); other shapes
+ *   return VATTN_ERR_UNSUPPORTED (round q to f16 and call vattn_forward_f16).
+ * Asynchronous, no allocation, one kernel launch; errors as for
+ * vattn_forward_f16.
+ */
+vattn_status vattn_forward_f32q(const float* q, const uint16_t* k, const uint16_t* v, float* out,
+                                int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, void* stream);
 
 /*
  * vattn_rope_neox -- NeoX rotary position embedding, in place.
@@ -275,11 +300,12 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
  * allocation in its execute step, or a latency-bound loop that cannot take an
  * allocation's cost or a late out-of-memory failure.
  *
- * Arguments, layout, result and error codes are those of vattn_forward.  The
- * f16 copies of q, k and v go to a fixed array of
- * VATTN_NOALLOC_MAX_SCRATCH_BYTES that the library's device code holds on
- * every device it is loaded on (for the life of the process), instead of a
- * pool allocation; the call makes no cudaMalloc/cudaFree-type call.
+ * Arguments, layout, result and error codes are those of vattn_forward, and
+ * so are its kernels.  The f16 copies that vattn_forward makes go to a
+ * fixed array of VATTN_NOALLOC_MAX_SCRATCH_BYTES that the library's device
+ * code holds on every device it is loaded on (for the life of the process),
+ * instead of a pool allocation; the call makes no cudaMalloc/cudaFree-type
+ * call.
  *
  * Limit: a problem whose f16 copies (3 x 256-byte-rounded
  * batch*n_heads*n_patches*round_up(head_dim, 16)*2 bytes) exceed the array is

@@ -19,6 +19,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = _lib.exported_symbols()
     assert set(names) == {"vattn_forward", "vattn_forward_f16", "vattn_forward_f16io",
+                          "vattn_forward_f32q",
                           "vattn_forward_noalloc", "vattn_forward_accurate",
                           "vattn_conv1d_step", "vattn_forward_host",
                           "vattn_selftest_wait_timeout",
@@ -90,6 +91,41 @@ def test_host_side_argument_errors(lib, args, status):
 def test_f16_entry_host_side_argument_errors(lib, args, status):
     assert _lib.forward_f16_status(*args, 0) == status
     assert lib.vattn_last_error_string().decode() != ""
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, -1, 2, 200, 64), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 200, 0), 1),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 200, 72), 2),    # head_dim > 64
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 200, 36), 2),    # head_dim % 8 != 0
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 128, 64), 2),    # one query tile
+    ((0, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 200, 64), 1),
+    ((FAKE + 8, FAKE, FAKE, FAKE + 2 ** 30, 1, 2, 200, 64), 3),  # q needs 16 bytes
+    ((FAKE, FAKE + 2 ** 24 + 2, FAKE, FAKE + 2 ** 30, 1, 2, 200, 64), 3),
+    ((FAKE, FAKE, FAKE, FAKE + 2 ** 30 + 2, 1, 2, 200, 64), 3),
+    ((FAKE, FAKE + 2 ** 24, FAKE + 2 ** 25, FAKE + 64, 1, 2, 200, 64), 1),  # out overlaps q
+    ((FAKE, FAKE, FAKE, FAKE, 1, 1, 2 ** 31, 64), 2),
+])
+def test_f32q_entry_host_side_argument_errors(lib, args, status):
+    assert _lib.forward_f32q_status(*args, 0) == status
+    assert lib.vattn_last_error_string().decode() != ""
+
+
+@pytest.mark.parametrize("b,h,n", [(0, 4, 10), (2, 0, 10), (2, 4, 0)])
+def test_f32q_entry_empty_problems_are_no_ops(lib, b, h, n):
+    assert _lib.forward_f32q_status(0, 0, 0, 0, b, h, n, 64, 0) == 0
+
+
+def test_f32q_binding_rejects_bad_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 2, 300, 64)
+    kv = q.half()
+    with pytest.raises(TypeError):
+        vef.forward_f32q(kv, kv, kv)   # q must be float32
+    with pytest.raises(TypeError):
+        vef.forward_f32q(q, q, kv)     # k must be float16
+    with pytest.raises(ValueError):
+        vef.forward_f32q(q, kv, kv)    # CPU tensors
 
 
 @pytest.mark.parametrize("b,h,n", [(0, 4, 10), (2, 0, 10), (2, 4, 0)])

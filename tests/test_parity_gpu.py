@@ -311,3 +311,51 @@ def test_direct_path_limit(torch_dev, n):
     got = run_gpu(torch_dev, q, k, v)
     rows = np.array([0, 1, 1023, n - 2, n - 1])  # one head: flat index = row
     assert_parity(got.reshape(-1, 64)[rows], oracle.rows(q, k, v, rows), f"limit N={n}")
+
+
+def run_gpu_offsets(torch_dev, q, k, v, offsets):
+    """vattn_forward with q, k, v (and out) starting offsets[i] f32 elements
+    past fresh allocations."""
+    torch, dev = torch_dev
+    numel = q.size
+    ptrs, keep = [], []
+    for x, off in zip((q, k, v), offsets):
+        t = torch.zeros(numel + 4, device=dev)
+        t[off:off + numel] = torch.from_numpy(x.ravel()).to(dev)
+        keep.append(t)
+        ptrs.append(t.data_ptr() + 4 * off)
+    out = torch.zeros(numel + 4, device=dev)
+    vef.forward_raw(*ptrs, out.data_ptr() + 16, *q.shape, torch.cuda.current_stream(dev).cuda_stream)
+    torch.cuda.synchronize(dev)
+    assert vef.device_status() == 0
+    return out[4:4 + numel].cpu().numpy().reshape(q.shape)
+
+
+# Two-pass shapes whose attention kernel rounds q itself (two query tiles,
+# head_dim <= 64 and a multiple of 4, q 16-byte aligned, past the direct
+# path's 2048 patches): the staging kernel rounds k and v only.
+Q_F32 = [(1, 2, 2049, 64), (1, 2, 2300, 36), (1, 3, 2500, 20), (2, 40, 2176, 64)]
+
+
+@pytest.mark.parametrize("shape", Q_F32)
+def test_query_f32_path(torch_dev, shape):
+    q, k, v = make_inputs(*shape, seed=5300 + shape[2] + shape[3])
+    got = run_gpu(torch_dev, q, k, v)
+    b, h, n, d = shape
+    rng = np.random.default_rng(n + d)
+    heads = np.arange(b * h) * n
+    rows = np.union1d(rng.choice(b * h * n, size=192, replace=False),
+                      np.concatenate([heads, heads + n - 1]))
+    sel = got.reshape(-1, d)[rows]
+    assert_kernel_arithmetic(sel, q, k, v, rows=rows, what=f"q f32 {shape}")
+    assert_parity(sel, oracle.rows(q, k, v, rows), f"q f32 {shape}", rel_l2=2 * MAX_REL_L2)
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 2049, 64), (2, 40, 2176, 64), (1, 3, 2500, 20)])
+def test_query_f32_and_staged_query_agree_bitwise(torch_dev, shape):
+    # q 16-byte aligned: the attention kernel rounds q; q 4-byte aligned only:
+    # the staging kernel does.  The same rounding either way: identical bits.
+    q, k, v = make_inputs(*shape, seed=5400 + shape[2])
+    a = run_gpu_offsets(torch_dev, q, k, v, (4, 4, 4))
+    b = run_gpu_offsets(torch_dev, q, k, v, (1, 4, 4))
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

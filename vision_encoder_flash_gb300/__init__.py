@@ -11,12 +11,13 @@ from __future__ import annotations
 
 from ._lib import (VattnError, _check, conv1d_step_status, device_status, exported_symbols,
                    forward_accurate_status, forward_host_status,
-                   forward_f16_raw, forward_f16io_status,
+                   forward_f16_raw, forward_f16io_status, forward_f32q_raw,
                    forward_noalloc_raw, forward_raw, forward_rope_status, lib_path,
                    load_library, rope_neox_status, status_string, version)
 
-__all__ = ["forward", "forward_accurate", "conv1d_step", "forward_f16", "forward_f16io", "forward_rope", "rope_neox", "forward_raw",
-           "forward_f16_raw", "forward_noalloc_raw",
+__all__ = ["forward", "forward_accurate", "conv1d_step", "forward_f16", "forward_f16io",
+           "forward_f32q", "forward_rope", "rope_neox", "forward_raw",
+           "forward_f16_raw", "forward_f32q_raw", "forward_noalloc_raw",
            "device_status", "VattnError", "load_library",
            "lib_path", "exported_symbols", "status_string", "version"]
 
@@ -102,6 +103,40 @@ def forward_f16(q, k, v, out=None, stream=None):
     B, H, N, D = q.shape
     forward_f16_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D,
                     s.cuda_stream)
+    return out
+
+
+def forward_f32q(q, k, v, out=None, stream=None):
+    """out (f32) = softmax(q k^T) v for a CUDA float32 ``q`` and float16 ``k``,
+    ``v`` of one shape ``[B, H, N, D]`` (``D`` a multiple of 8 and at most 64,
+    ``N`` > 128); the kernel rounds q to f16 itself.  Runs on ``stream``
+    (default: the current torch stream) and returns ``out`` without
+    synchronising."""
+    import torch
+
+    for name, t, dt in (("q", q, torch.float32), ("k", k, torch.float16), ("v", v, torch.float16)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [batch, n_heads, n_patches, head_dim]")
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (head-major [B, H, N, D])")
+    if not (q.shape == k.shape == v.shape) or not (q.device == k.device == v.device):
+        raise ValueError("q, k and v must have one shape and one device")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.float32 or out.device != q.device \
+            or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor of q's shape and device")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    B, H, N, D = q.shape
+    forward_f32q_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D,
+                     s.cuda_stream)
     return out
 
 

@@ -47,6 +47,8 @@ def load_library():
     lib.vattn_forward_f16io.restype = ctypes.c_int
     lib.vattn_forward_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_f16.restype = ctypes.c_int
+    lib.vattn_forward_f32q.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.vattn_forward_f32q.restype = ctypes.c_int
     lib.vattn_forward_accurate.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_accurate.restype = ctypes.c_int
     lib.vattn_conv1d_step.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
@@ -101,6 +103,20 @@ def forward_f16_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, 
     """Like forward_f16_raw but returns the status code instead of raising."""
     return int(load_library().vattn_forward_f16(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                                 n_patches, head_dim, stream))
+
+
+def forward_f32q_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, batch: int, n_heads: int,
+                     n_patches: int, head_dim: int, stream: int = 0) -> None:
+    """Direct call of vattn_forward_f32q: f32 q, f16 k and v (device addresses), f32 out."""
+    _check(load_library().vattn_forward_f32q(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                             n_patches, head_dim, stream))
+
+
+def forward_f32q_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,
+                        stream=0) -> int:
+    """Like forward_f32q_raw but returns the status code instead of raising."""
+    return int(load_library().vattn_forward_f32q(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                                 n_patches, head_dim, stream))
 
 
 def forward_f16io_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim,

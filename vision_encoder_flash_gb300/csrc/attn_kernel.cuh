@@ -100,11 +100,20 @@ struct Params {
 // f16 tiles: NKB blocks of [128 rows x 128 bytes], 128-byte swizzle.
 // kAcc (accurate mode, one query tile): every Q, K and V tile comes as an
 // f16 pair (hi, lo), the lo part right after the hi part.
-// kF32 (f32 inputs, two query tiles, head_dim <= 64): q, k and v tiles come
-// in as f32 [128 rows x 64 columns] into a ring of two slots, and a fourth
-// warpgroup rounds them to f16 into the same swizzled tiles.
-template <int NQ, int NKB, bool kAcc = false, bool kF32 = false>
+// kIn (two query tiles, head_dim <= 64 for kInF32 and kInF32Q): where the
+// operands come from.
+//   kInF16:  q, k, v f16 copies (the staging kernel's), TMA into the tiles;
+//   kInF32:  q, k, v f32 tiles [128 rows x 64 columns] into a ring of three
+//            slots; a fourth warpgroup rounds them to f16 into the same
+//            swizzled tiles;
+//   kInF32Q: k, v f16 copies; q f32 tiles into two slots (one per query
+//            tile), rounded to f16 by warp 3 once per work tile.
+constexpr int kInF16 = 0, kInF32 = 1, kInF32Q = 2;
+
+template <int NQ, int NKB, bool kAcc = false, int kIn = kInF16>
 struct Plan {
+  static constexpr bool kF32 = kIn == kInF32;    // every operand from f32
+  static constexpr bool kF32Q = kIn == kInF32Q;  // q from f32
   // control warpgroup + one softmax warpgroup per query tile (+ converters)
   static constexpr int kThreads = 128 * (1 + NQ) + (kF32 ? 128 : 0);
   static constexpr int kTileF16 = NKB * kBoxBytes;
@@ -112,7 +121,7 @@ struct Plan {
   static constexpr int kPartBytes = kTileF16;      // offset of lo after hi
   static constexpr int kStageStride = kParts * kTileF16;
   static constexpr int kStages =  // K and V stages
-      kF32 ? 2 : (kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3)));
+      kF32 ? 2 : (kF32Q ? 3 : (kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3))));
   // two query tiles with head_dim > 64: O needs 2 x 80..128 TMEM columns, so
   // the two tiles take turns with one P buffer
   static constexpr bool kSharedP = NQ == 2 && NKB == 2;
@@ -123,7 +132,7 @@ struct Plan {
   // 2 KB buffers (32 rows x 16 f32, 64-byte swizzle) per softmax warp
   static constexpr int kEpiBytes = (NKB == 1 && !kAcc) ? 4 * NQ * 4096 : 0;
   static constexpr int kOffEpi = kOffV + kStages * kStageStride;
-  static constexpr int kF32Slots = kF32 ? 3 : 0;
+  static constexpr int kF32Slots = kF32 ? 3 : (kF32Q ? NQ : 0);
   static constexpr int kF32TileBytes = kBM * 64 * 4;  // 128 rows x 64 f32, unswizzled
   static constexpr int kOffF32 = kOffEpi + kEpiBytes;
   static constexpr int kOffBar = kOffF32 + kF32Slots * kF32TileBytes;
@@ -149,7 +158,8 @@ struct Plan {
   static_assert(!kSplitRegs || (kF32 ? 2 : 1) * kRegsOther + NQ * kRegsSoftmax <=
                                     static_cast<uint32_t>(kThreads / 128) * kRegsLaunch,
                 "register split too large");
-  static_assert(!kF32 || (NQ == 2 && NKB == 1 && !kAcc), "f32 inputs: two query tiles, head_dim <= 64");
+  static_assert(kIn == kInF16 || (NQ == 2 && NKB == 1 && !kAcc),
+                "f32 inputs: two query tiles, head_dim <= 64");
   static_assert(kF32Slots <= 4, "f32 ring barriers");
   static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
   static_assert(!kSharedP || !kAcc, "shared P is for the f16 path");
@@ -172,7 +182,8 @@ enum Bar : int {
   kBarQEmpty = 30,    // S products of a tile done with its Q tiles (commit)
   kBarF32Full = 31,   // [4] f32 ring slot landed           (1 + tx)
   kBarF32Empty = 35,  // [4] f32 ring slot read (one per converter warp)
-  kNumBars = 39,
+  kBarQFull1 = 39,    // kInF32Q: Q tile 1 rounded (Q tile 0: kBarQFull)
+  kNumBars = 40,
 };
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
 constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
@@ -237,13 +248,17 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
 // into P hi and P lo, and each product takes three MMAs:
 //   S = Qh Kh^T + Qh Kl^T + Ql Kh^T,   O += Ph Vh + Ph Vl + Pl Vh
 // (the lo x lo terms are below 2^-22 relative).
-// kF32: tm_q / tm_k / tm_v are f32 [B*H, N, head_dim] maps with boxes of
-// {64 columns, 128 rows}, no swizzle (head_dim % 4 == 0, <= 64); warp 0
-// streams the tiles (per work tile: K_0, V_0, Q_0, Q_1, K_1, V_1, ...) into
-// a two-slot f32 ring, and warps 12..15 round each one to f16 into its
-// swizzled Q, K or V tile (the f16 staging pass is not needed).
-template <int NQ, int NKB, bool kOut16 = false, bool kAcc = false, bool kF32 = false>
-__global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
+// kIn == kInF32: tm_q / tm_k / tm_v are f32 [B*H, N, head_dim] maps with
+// boxes of {64 columns, 128 rows}, no swizzle (head_dim % 4 == 0, <= 64);
+// warp 0 streams the tiles (per work tile: K_0, V_0, Q_0, Q_1, K_1, V_1, ...)
+// into the f32 ring, and warps 12..15 round each one to f16 into its swizzled
+// Q, K or V tile (the f16 staging pass is not needed).
+// kIn == kInF32Q: tm_q is such an f32 map and tm_k / tm_v the f16 ones; warp
+// 3 loads the next work tile's Q tiles into their f32 slots while the
+// current one runs and rounds them into the Q tiles once the S products are
+// done with the old ones (the staging pass then only rounds k and v).
+template <int NQ, int NKB, bool kOut16 = false, bool kAcc = false, int kIn = kInF16>
+__global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
     vattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
@@ -251,7 +266,9 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_ql,
                      const __grid_constant__ CUtensorMap tm_kl,
                      const __grid_constant__ CUtensorMap tm_vl, const Params p) {
-  using P = Plan<NQ, NKB, kAcc, kF32>;
+  using P = Plan<NQ, NKB, kAcc, kIn>;
+  constexpr bool kF32 = P::kF32;
+  constexpr int kRing = P::kF32Slots > 0 ? P::kF32Slots : 1;  // f32 ring size (index arithmetic)
   constexpr int S = P::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = ptx::smem_addr(smem_raw);
@@ -290,7 +307,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     // f32 inputs: the converter warps (four) arrive on the f16 tiles' barriers
-    ptx::mbar_init(bar(kBarQFull), kF32 ? 4 * NQ : 1);
+    ptx::mbar_init(bar(kBarQFull), kF32 ? 4 * NQ : 1);  // kInF32Q: warp 3, Q tile 0
+    ptx::mbar_init(bar(kBarQFull1), 1);                 // kInF32Q: warp 3, Q tile 1
     ptx::mbar_init(bar(kBarQEmpty), 1);
     for (int i = 0; i < S; ++i) {
       ptx::mbar_init(bar(kBarKFull + i), kF32 ? 4 : 1);
@@ -336,8 +354,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
     const int cw = warp - (4 + 4 * NQ);
     int64_t n = 0;
     auto convert = [&](uint32_t dst, int full_bar) -> bool {
-      const int slot = static_cast<int>(n % P::kF32Slots);
-      if (!w.wait_warp(bar(kBarF32Full + slot), static_cast<uint32_t>((n / P::kF32Slots) & 1),
+      const int slot = static_cast<int>(n % kRing);
+      if (!w.wait_warp(bar(kBarF32Full + slot), static_cast<uint32_t>((n / kRing) & 1),
                        kSiteConvert))
         return false;
       const uint32_t src = base_s + P::kOffF32 + static_cast<uint32_t>(slot * P::kF32TileBytes);
@@ -391,9 +409,9 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
         ptx::grid_dep_wait();  // the previous kernel's writes of q, k, v are visible
         int64_t n = 0;
         auto load = [&](const CUtensorMap* tm, int row0, int bh) -> bool {
-          const int slot = static_cast<int>(n % P::kF32Slots);
+          const int slot = static_cast<int>(n % kRing);
           if (!w.wait(bar(kBarF32Empty + slot),
-                      static_cast<uint32_t>(((n / P::kF32Slots) & 1) ^ 1), kSiteProducerK))
+                      static_cast<uint32_t>(((n / kRing) & 1) ^ 1), kSiteProducerK))
             return false;
           ptx::mbar_arrive_expect_tx(bar(kBarF32Full + slot), P::kF32TileBytes);
           ptx::tma_load_3d(base_s + P::kOffF32 + static_cast<uint32_t>(slot * P::kF32TileBytes),
@@ -411,9 +429,9 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
           }
         }
         // every issued copy must have landed before the block exits
-        for (int64_t m = (n > P::kF32Slots ? n - P::kF32Slots : 0); m < n; ++m)
-          w.drain(bar(kBarF32Full + static_cast<int>(m % P::kF32Slots)),
-                  static_cast<uint32_t>((m / P::kF32Slots) & 1), kSiteDrainTma);
+        for (int64_t m = (n > kRing ? n - kRing : 0); m < n; ++m)
+          w.drain(bar(kBarF32Full + static_cast<int>(m % kRing)),
+                  static_cast<uint32_t>((m / kRing) & 1), kSiteDrainTma);
       }
     } else if (warp == 0) {
       // ------------------------------------------------- K/V producer
@@ -465,6 +483,66 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
         for (int64_t g = (v_issued > S ? v_issued - S : 0); g < v_issued; ++g)
           w.drain(bar(kBarVFull + kv_stage(g)), kv_phase(g), kSiteDrainTma);
       }
+    } else if (warp == 3 && P::kF32Q) {
+      // ----------------------------------------- Q from f32, rounded here
+      // Q_t of tile i comes by TMA into f32 slot t while tile i - 1 runs;
+      // once the S products of tile i - 1 are done with the Q tiles, the
+      // warp rounds slot t into Q tile t (four rows per step, 8 lanes per
+      // row, eight f32 columns per lane, one 16-byte unit of the
+      // 128-byte-swizzled f16 layout each), tells the S issuer that tile t
+      // is ready and reloads slot t with the next tile's Q_t.
+      auto load_q = [&](int i, int t) {
+        ptx::mbar_arrive_expect_tx(bar(kBarF32Full + t), P::kF32TileBytes);
+        ptx::tma_load_3d(base_s + P::kOffF32 + static_cast<uint32_t>(t * P::kF32TileBytes), &tm_q,
+                         bar(kBarF32Full + t), 0, tile_row0(i) + t * kBM, tile_bh(i));
+      };
+      if (lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::grid_dep_wait();
+        for (int t = 0; t < NQ; ++t) load_q(0, t);
+      }
+      int q_loaded[NQ];  // per slot: tiles whose Q load was issued (lane 0)
+      for (int t = 0; t < NQ; ++t) q_loaded[t] = 1;
+      bool ok = true;
+      const int u = lane & 7;  // f32 columns 8 u .. 8 u + 7 = 16-byte f16 unit u
+      for (int i = 0; ok && i < n_mine; ++i) {
+        if (i > 0 && !(ok = w.wait_warp(bar(kBarQEmpty), static_cast<uint32_t>(i - 1) & 1u,
+                                        kSiteProducerQ)))
+          break;
+        for (int t = 0; ok && t < NQ; ++t) {
+          if (!(ok = w.wait_warp(bar(kBarF32Full + t), static_cast<uint32_t>(i) & 1u, kSiteConvert)))
+            break;
+          const uint32_t src = base_s + P::kOffF32 + static_cast<uint32_t>(t * P::kF32TileBytes);
+          const uint32_t dst = base_s + P::kOffQ + static_cast<uint32_t>(t * P::kStageStride);
+#pragma unroll 4
+          for (int it = 0; it < kBM / 4; ++it) {
+            const int r = 4 * it + (lane >> 3);
+            const uint32_t a = src + static_cast<uint32_t>(r * 256 + u * 32);
+            const float4 x0 = ptx::ld_shared_v4(a);
+            const float4 x1 = ptx::ld_shared_v4(a + 16u);
+            ptx::st_shared_v4(dst + static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4)),
+                              __uint_as_float(ptx::pack_half2(x0.x, x0.y)),
+                              __uint_as_float(ptx::pack_half2(x0.z, x0.w)),
+                              __uint_as_float(ptx::pack_half2(x1.x, x1.y)),
+                              __uint_as_float(ptx::pack_half2(x1.z, x1.w)));
+          }
+          // the tensor core reads Q tile t, and the next TMA writes slot t,
+          // after this warp's shared-memory accesses
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive(bar(t == 0 ? kBarQFull : kBarQFull1));
+            if (i + 1 < n_mine) {
+              load_q(i + 1, t);
+              ++q_loaded[t];
+            }
+          }
+        }
+      }
+      // every issued copy must have landed before the block exits
+      if (lane == 0)
+        for (int t = 0; t < NQ; ++t)
+          w.drain(bar(kBarF32Full + t), static_cast<uint32_t>(q_loaded[t] - 1) & 1u, kSiteDrainTma);
     } else if (warp == 3 && !kF32) {
       // --------------------------------------------------- Q producer
       // The Q tiles of tile i go in as soon as the S products of tile i-1
@@ -534,7 +612,14 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kF32>::kThreads, 1)
                 !(ok = w.wait(bar(kBarSFree + sfree_bar(prev)), sphase(prev), kSiteMmaSFree)))
               break;
             ptx::tc_fence_after();
-            for (int t = 0; t < NQ; ++t) issue_s(t, g);
+            for (int t = 0; t < NQ; ++t) {
+              if (P::kF32Q && j == 0 && t == 1) {  // Q tile 1 is rounded after tile 0
+                if (!(ok = w.wait(bar(kBarQFull1), static_cast<uint32_t>(i) & 1u, kSiteMmaQ))) break;
+                ptx::tc_fence_after();
+              }
+              issue_s(t, g);
+            }
+            if (!ok) break;
             ptx::mma_commit(bar(kBarKEmpty + kv_stage(g)));
           }
           // the Q tiles are free once these S products have run

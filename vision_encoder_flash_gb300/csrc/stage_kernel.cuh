@@ -25,16 +25,17 @@ struct StageJob {
   __half* dst;
 };
 
-// Three tensors (q, k, v) of n_rows x D each.  Thread i handles 8-column
-// chunks i, i + stride, ... of the concatenated [3 * n_rows, d_pad / 8]
-// chunk grid.  vec: D % 8 == 0 and 16-byte aligned sources -> two 16-byte
-// loads per chunk; otherwise element loads.
+// n_jobs (2 or 3) tensors (a, b[, c]: q, k, v, or k and v alone when the
+// attention kernel rounds q itself) of n_rows x D each.  Thread i handles
+// 8-column chunks i, i + stride, ... of the concatenated
+// [n_jobs * n_rows, d_pad / 8] chunk grid.  vec: D % 8 == 0 and 16-byte
+// aligned sources -> two 16-byte loads per chunk; otherwise element loads.
 __global__ void __launch_bounds__(256) vattn_stage_kernel(StageJob a, StageJob b, StageJob c,
-                                                         long long n_rows, int D, int d_pad,
-                                                         int vec) {
+                                                         int n_jobs, long long n_rows, int D,
+                                                         int d_pad, int vec) {
   const int cpr = d_pad >> 3;
   const long long chunks_per_tensor = n_rows * cpr;
-  const long long total = 3 * chunks_per_tensor;
+  const long long total = n_jobs * chunks_per_tensor;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += stride) {

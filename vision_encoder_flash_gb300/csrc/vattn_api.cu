@@ -187,14 +187,14 @@ vattn_status sm_count(int device, int* out) {
 // one per tile), each looping over the tiles blockIdx.x + k * gridDim.x.
 // tql, tkl, tvl: the lo halves of q, k, v (accurate mode only; otherwise
 // unused and any valid map may be passed).
-template <int NQ, int NKB, bool kOut16, bool kAcc, bool kF32 = false>
+template <int NQ, int NKB, bool kOut16, bool kAcc, int kIn = vattn::kInF16>
 vattn_status launch_attention_maps(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const CUtensorMap& tql,
                                    const CUtensorMap& tkl, const CUtensorMap& tvl,
                                    vattn::Params p, unsigned n_tiles, cudaStream_t stream,
                                    int device) {
-  using P = vattn::Plan<NQ, NKB, kAcc, kF32>;
-  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kOut16, kAcc, kF32>;
+  using P = vattn::Plan<NQ, NKB, kAcc, kIn>;
+  auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kOut16, kAcc, kIn>;
   static std::atomic<uint8_t> configured[kMaxDevices];
   if (!configured[device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -288,8 +288,8 @@ vattn_status launch_f32_direct(const float* q, const float* k, const float* v, f
   if ((st = make_tmap32(&tq, q, bh, N, D)) != VATTN_OK) return st;
   if ((st = make_tmap32(&tk, k, bh, N, D)) != VATTN_OK) return st;
   if ((st = make_tmap32(&tv, v, bh, N, D)) != VATTN_OK) return st;
-  return launch_attention_maps<2, 1, false, false, true>(tq, tk, tv, tq, tk, tv, p,
-                                                         static_cast<unsigned>(grid), stream, device);
+  return launch_attention_maps<2, 1, false, false, vattn::kInF32>(
+      tq, tk, tv, tq, tk, tv, p, static_cast<unsigned>(grid), stream, device);
 }
 
 // The kernel variant for nkb 64-column blocks of d_pad and nq query tiles.
@@ -488,8 +488,12 @@ vattn_status launch_conv1d4(const vattn::Conv1dArgs& a, int device, int sms, cud
                           sms, stream);
 }
 
-// The two kernels of vattn_forward on device tensors of bh heads, with the
-// f16 workspace ws (three regions of `region` bytes) supplied by the caller.
+// The kernels of vattn_forward on device tensors of bh heads, with the f16
+// workspace ws (three regions of `region` bytes) supplied by the caller:
+// the direct f32 kernel where it applies, else the staging kernel and the
+// attention kernel.  With two query tiles of head_dim <= 64 the attention
+// kernel reads q in f32 and rounds it itself (q is read once per work tile,
+// so that costs it little) and the staging kernel rounds k and v alone.
 // Arguments are valid (checked by the entry points).
 vattn_status run_forward(const float* q, const float* k, const float* v, float* out, int64_t bh,
                          int N, int D, void* ws, size_t region, cudaStream_t stream, int device) {
@@ -509,26 +513,38 @@ vattn_status run_forward(const float* q, const float* k, const float* v, float* 
   p.n_tiles = static_cast<int>(grid);
   p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
   p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  const bool q_f32 = nkb == 1 && nq == 2 && D % 4 == 0 && (reinterpret_cast<uintptr_t>(q) & 15u) == 0;
   __half* q16 = static_cast<__half*>(ws);
   __half* k16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + region);
   __half* v16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + 2 * region);
   CUtensorMap tq, tk, tv;
   vattn_status st;
-  if ((st = make_tmap16(&tq, q16, bh, N, d_pad)) != VATTN_OK) return st;
+  if ((st = q_f32 ? make_tmap32(&tq, q, bh, N, D) : make_tmap16(&tq, q16, bh, N, d_pad)) != VATTN_OK)
+    return st;
   if ((st = make_tmap16(&tk, k16, bh, N, d_pad)) != VATTN_OK) return st;
   if ((st = make_tmap16(&tv, v16, bh, N, d_pad)) != VATTN_OK) return st;
   const int64_t rows = bh * N;
-  const int vec = (D % 8 == 0) &&
-                  ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                    reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
-  const long long chunks = 3LL * rows * (d_pad / 8);
+  const uintptr_t src_or = (q_f32 ? 0u : reinterpret_cast<uintptr_t>(q)) |
+                           reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v);
+  const int vec = (D % 8 == 0) && (src_or & 15u) == 0;
+  const int n_jobs = q_f32 ? 2 : 3;
+  const long long chunks = n_jobs * rows * (d_pad / 8);
   const long long blocks = (chunks + 255) / 256;
   const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
-  vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
-      vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, rows, D, d_pad, vec);
+  if (q_f32)
+    vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
+        vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, vattn::StageJob{nullptr, nullptr}, 2, rows,
+        D, d_pad, vec);
+  else
+    vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
+        vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, 3, rows, D,
+        d_pad, vec);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
   const unsigned g = static_cast<unsigned>(grid);
+  if (q_f32)
+    return launch_attention_maps<2, 1, false, false, vattn::kInF32Q>(tq, tk, tv, tq, tk, tv, p, g,
+                                                                      stream, device);
   return dispatch_attention(nkb, nq, tq, tk, tv, p, g, stream, device);
 }
 
@@ -596,25 +612,9 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   chk = check_attention_tensors(q, k, v, out, batch, n_heads, n_patches, head_dim, &bh, &empty);
   if (chk != VATTN_OK) return chk;
   if (empty) return VATTN_OK;  // nothing to compute
-
   const int D = static_cast<int>(head_dim);
   const int N = static_cast<int>(n_patches);
   const int d_pad = (D + 15) & ~15;
-  const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = query_tiles(N, d_pad);
-  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
-  const int64_t grid = bh * n_qblocks;
-  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
-
-  vattn::Params p{};
-  p.out = out;
-  p.n_patches = N;
-  p.head_dim = D;
-  p.d_pad = d_pad;
-  p.n_qblocks = static_cast<int>(n_qblocks);
-  p.n_tiles = static_cast<int>(grid);
-  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
-  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
 
   // ---- device side
   int device = 0;
@@ -623,40 +623,16 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (f32_direct(q, k, v, N, D)) return launch_f32_direct(q, k, v, out, bh, N, D, stream, device);
 
-  // f16 copies of q, k, v ([B*H, N, d_pad] each), stream-ordered workspace
-  const int64_t rows = bh * N;
-  const size_t region = (static_cast<size_t>(rows) * d_pad * 2 + 255) & ~static_cast<size_t>(255);
+  // f16 copies ([B*H, N, d_pad] each), stream-ordered workspace
+  const size_t region =
+      (static_cast<size_t>(bh) * N * d_pad * 2 + 255) & ~static_cast<size_t>(255);
   cudaMemPool_t pool = nullptr;
   vattn_status st = pool_for(device, &pool);
   if (st != VATTN_OK) return st;
   void* ws = nullptr;
   e = cudaMallocFromPoolAsync(&ws, 3 * region, pool, stream);
   if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
-  __half* q16 = static_cast<__half*>(ws);
-  __half* k16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + region);
-  __half* v16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + 2 * region);
-
-  CUtensorMap tq, tk, tv;
-  if ((st = make_tmap16(&tq, q16, bh, N, d_pad)) == VATTN_OK &&
-      (st = make_tmap16(&tk, k16, bh, N, d_pad)) == VATTN_OK &&
-      (st = make_tmap16(&tv, v16, bh, N, d_pad)) == VATTN_OK) {
-    const int vec = (D % 8 == 0) &&
-                    ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                      reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
-    const long long chunks = 3LL * rows * (d_pad / 8);
-    const long long blocks = (chunks + 255) / 256;
-    const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
-    vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
-        vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, rows, D, d_pad,
-        vec);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) {
-      st = cuda_fail(e, "staging kernel launch");
-    } else {
-      const unsigned g = static_cast<unsigned>(grid);
-      st = dispatch_attention(nkb, nq, tq, tk, tv, p, g, stream, device);
-    }
-  }
+  st = run_forward(q, k, v, out, bh, N, D, ws, region, stream, device);
   // back to the pool once the launches above have run (stream order)
   e = cudaFreeAsync(ws, stream);
   if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
@@ -673,6 +649,72 @@ vattn_status vattn_forward_f16io(const uint16_t* q, const uint16_t* k, const uin
                                  uint16_t* out, int64_t batch, int64_t n_heads,
                                  int64_t n_patches, int64_t head_dim, void* stream_ptr) {
   return forward_f16_impl<true>(q, k, v, out, batch, n_heads, n_patches, head_dim, stream_ptr);
+}
+
+vattn_status vattn_forward_f32q(const float* q, const uint16_t* k, const uint16_t* v, float* out,
+                                int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, void* stream_ptr) {
+  g_last_error[0] = '\0';
+  // ---- host-side checks, before any CUDA call
+  vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  if (head_dim % 8 != 0 || head_dim > 64)
+    return fail(VATTN_ERR_UNSUPPORTED,
+                "f32 q with f16 k, v needs head_dim %% 8 == 0 and <= 64, got %lld: use "
+                "vattn_forward_f16 with q rounded to f16",
+                (long long)head_dim);
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  const int64_t bh = batch * n_heads;
+  if (bh == 0 || n_patches == 0) return VATTN_OK;  // nothing to compute
+  if (n_patches <= vattn::kBM)
+    return fail(VATTN_ERR_UNSUPPORTED,
+                "f32 q with f16 k, v needs n_patches > %d, got %lld: use vattn_forward_f16 with q "
+                "rounded to f16",
+                vattn::kBM, (long long)n_patches);
+  if (!q || !k || !v || !out) return fail(VATTN_ERR_INVALID_ARG, "null tensor pointer");
+  if (n_patches > INT32_MAX || bh > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  if (n_patches > INT64_MAX / head_dim / bh / 4)
+    return fail(VATTN_ERR_UNSUPPORTED, "tensor byte size overflows");
+  const uint64_t f32_bytes = static_cast<uint64_t>(bh) * n_patches * head_dim * 4u;
+  const uint64_t f16_bytes = f32_bytes / 2u;
+  if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+        reinterpret_cast<uintptr_t>(v)) & 15u) != 0)
+    return fail(VATTN_ERR_MISALIGNED, "q, k, v must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(out) & 3u)
+    return fail(VATTN_ERR_MISALIGNED, "out must be 4-byte aligned");
+  if (overlaps(out, q, f32_bytes) || overlaps2(out, f32_bytes, k, f16_bytes) ||
+      overlaps2(out, f32_bytes, v, f16_bytes))
+    return fail(VATTN_ERR_INVALID_ARG, "out overlaps q, k or v");
+
+  const int D = static_cast<int>(head_dim);
+  const int N = static_cast<int>(n_patches);
+  const int64_t n_qblocks = (N + 2 * vattn::kBM - 1) / (2 * vattn::kBM);
+  const int64_t grid = bh * n_qblocks;
+  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+  vattn::Params p{};
+  p.out = out;
+  p.n_patches = N;
+  p.head_dim = D;
+  p.d_pad = (D + 15) & ~15;
+  p.n_qblocks = static_cast<int>(n_qblocks);
+  p.n_tiles = static_cast<int>(grid);
+  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.vec_out = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+
+  // ---- device side
+  int device = 0;
+  const cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  CUtensorMap tq, tk, tv;
+  vattn_status st;
+  if ((st = make_tmap32(&tq, q, bh, N, D)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tk, reinterpret_cast<const __half*>(k), bh, N, D)) != VATTN_OK) return st;
+  if ((st = make_tmap16(&tv, reinterpret_cast<const __half*>(v), bh, N, D)) != VATTN_OK) return st;
+  return launch_attention_maps<2, 1, false, false, vattn::kInF32Q>(
+      tq, tk, tv, tq, tk, tv, p, static_cast<unsigned>(grid), static_cast<cudaStream_t>(stream_ptr),
+      device);
 }
 
 vattn_status vattn_rope_neox(float* x, int64_t batch, int64_t n_heads, int64_t n_patches,
@@ -1191,54 +1233,17 @@ extern "C" vattn_status vattn_forward_noalloc(const float* q, const float* k, co
                 "round_up(head_dim, 16) x 2); vattn_forward_noalloc has %llu "
                 "(VATTN_NOALLOC_MAX_SCRATCH_BYTES): call vattn_forward instead",
                 (unsigned long long)(3u * region), (unsigned long long)kNoAllocScratchBytes);
-  const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = query_tiles(N, d_pad);
-  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
-  const int64_t grid = bh * n_qblocks;
-  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
-
-  vattn::Params p{};
-  p.out = out;
-  p.n_patches = N;
-  p.head_dim = D;
-  p.d_pad = d_pad;
-  p.n_qblocks = static_cast<int>(n_qblocks);
-  p.n_tiles = static_cast<int>(grid);
-  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
-  p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
-
   // ---- device side
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   uint8_t* ws = nullptr;
-  vattn_status st = noalloc_scratch(device, &ws);
+  const vattn_status st = noalloc_scratch(device, &ws);
   if (st != VATTN_OK) return st;
-  __half* q16 = reinterpret_cast<__half*>(ws);
-  __half* k16 = reinterpret_cast<__half*>(ws + region);
-  __half* v16 = reinterpret_cast<__half*>(ws + 2 * region);
-
-  CUtensorMap tq, tk, tv;
-  if ((st = make_tmap16(&tq, q16, bh, N, d_pad)) != VATTN_OK) return st;
-  if ((st = make_tmap16(&tk, k16, bh, N, d_pad)) != VATTN_OK) return st;
-  if ((st = make_tmap16(&tv, v16, bh, N, d_pad)) != VATTN_OK) return st;
-
   // Nothing in the scratch has to start at zero: the staging kernel writes
   // every f16 element the attention kernel reads (padding columns included),
   // and rows past n_patches are never read from memory (the tensor maps
-  // return zeros there).
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const int vec = (D % 8 == 0) &&
-                  ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                    reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
-  const long long chunks = 3LL * rows * (d_pad / 8);
-  const long long blocks = (chunks + 255) / 256;
-  const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
-  vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
-      vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, rows, D, d_pad,
-      vec);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
-  const unsigned g = static_cast<unsigned>(grid);
-  return dispatch_attention(nkb, nq, tq, tk, tv, p, g, stream, device);
+  // return zeros there).  Shapes of the direct f32 kernel use no scratch.
+  return run_forward(q, k, v, out, bh, N, D, ws, static_cast<size_t>(region),
+                     static_cast<cudaStream_t>(stream_ptr), device);
 }
