@@ -329,17 +329,22 @@ def run_vattn(args, workload):
     flops = float(workload.flops)
     value = weak_scaling_value(flops, world, ms_per_step)
 
-    # ---- the dominant kernel alone.  Past 2048 patches (head_dim <= 64) a
-    # step is the staging of k and v to f16, then the attention kernel that
-    # reads q in f32: vattn_forward_f32q launches exactly that kernel, here on
-    # k and v rounded to f16 once beforehand (untimed); per-launch events on
-    # the same stream.  (Up to 2048 patches the step is one kernel already.)
+    # ---- the dominant kernel alone.  With head_dim <= 64 (a multiple of 4)
+    # and more than 128 patches a step is one attention kernel (which rounds
+    # q, k and v to f16 itself; past 2048 patches after clearing its key-tile
+    # flags with a memset), so the step's own CUDA events time it.  Otherwise
+    # a step is the staging kernel and then the attention kernel; that one is
+    # timed alone through vattn_forward_f32q on k and v rounded to f16 once
+    # beforehand (untimed), per-launch events on the same stream.
     d_pad = (D + 15) // 16 * 16
-    one_kernel = 128 < N <= 2048 and 32 < D <= 64 and D % 4 == 0
+    one_kernel = N > 128 and D <= 64 and D % 4 == 0
     if one_kernel:
         attn_ms = launch_ms
         n_attn = len(launch_ms)
-        kernel_what = "vattn_fwd_kernel<2, 1, 0, 0, kInF32> (the whole call is this one kernel)"
+        kernel_what = (("vattn_fwd_kernel<2, 1, 0, 0, kInStageKV>" if N > 2048 else
+                        "vattn_fwd_kernel<2, 1, 0, 0, kInF32>") +
+                       " (the whole call is this one kernel; its CUDA events also hold the "
+                       "launch gap" + (" and the flag memset)" if N > 2048 else ")"))
     else:
         k16, v16 = kd.half(), vd.half()
         ptrs = (qd.data_ptr(), k16.data_ptr(), v16.data_ptr(), out.data_ptr(), B, H, N, D, sp)
@@ -531,12 +536,13 @@ def run_vattn(args, workload):
                      "kernel_ms_p10_p50_p90": [round(x, 5) for x in percentiles(attn_ms)],
                      "frac_of_sustained": achieved / (float(pk.get("bf16_tflops_sustained", peak_tf))
                                                       * F16_OVER_BF16_NOMINAL),
-                     "stage_kernel": {"bound": "hbm", "ms": stage_ms, "bytes": stage_bytes,
-                                      "achieved_gbs": stage_bytes / (stage_ms * 1e-3) / 1e9,
-                                      "peak_gbs": float(pk["hbm_gbs"]),
-                                      "frac": stage_bytes / (stage_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
-                                      "what": "vattn_stage_kernel on k and v (f32 in, f16 out)",
-                                      "how": "per-call time minus the attention kernel's time"}},
+                     "stage_kernel": None if one_kernel else {
+                         "bound": "hbm", "ms": stage_ms, "bytes": stage_bytes,
+                         "achieved_gbs": stage_bytes / (stage_ms * 1e-3) / 1e9,
+                         "peak_gbs": float(pk["hbm_gbs"]),
+                         "frac": stage_bytes / (stage_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
+                         "what": "vattn_stage_kernel on k and v (f32 in, f16 out)",
+                         "how": "per-call time minus the attention kernel's time"}},
         "cpu_baseline": cpu_baseline,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

@@ -56,18 +56,25 @@ typedef enum {
  *
  * The call is asynchronous: it validates arguments, launches its kernels on
  * `stream` and returns; the result is ready when the stream reaches that
- * point.  Two paths, the same f16 rounding and bit-identical results:
+ * point.  Three paths, the same f16 rounding and bit-identical results:
  *   - 128 < n_patches <= 2048, head_dim 33..64 and a multiple of 4, q, k, v
  *     16-byte aligned: one kernel that reads the f32 tiles and rounds them
  *     to f16 in shared memory; nothing is allocated;
+ *   - n_patches > 2048 with head_dim <= 64 and a multiple of 4 and q, k, v
+ *     16-byte aligned (also head_dim <= 32 from 129 patches on): a memset
+ *     and one cooperative kernel that writes the f16 copies of k and v
+ *     itself, each key tile once, while its blocks compute (a block reads a
+ *     key tile once the block that wrote it has set the tile's flag), and
+ *     rounds q itself;
  *   - otherwise two kernels (the f16 staging of q, k and v, then the
- *     attention kernel; with head_dim <= 64 and a multiple of 4, more than
- *     128 patches and q 16-byte aligned, the attention kernel rounds q
- *     itself and the staging kernel only k and v).  The f16 copies
- *     (at most 3 * batch*n_heads*n_patches*round_up(head_dim, 16) * 2
- *     bytes) live in a workspace taken stream-ordered from a memory pool the
- *     library keeps per device (cudaMallocFromPoolAsync / cudaFreeAsync on
- *     `stream`; the pool keeps its memory between calls).
+ *     attention kernel; the attention kernel rounds q itself when head_dim
+ *     <= 64 and q is 16-byte aligned, and the staging kernel then k and v
+ *     only).
+ *   The f16 copies and flags (at most 3 * batch*n_heads*n_patches*
+ *   round_up(head_dim, 16) * 2 bytes) live in a workspace taken
+ *   stream-ordered from a memory pool the library keeps per device
+ *   (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`; the pool keeps
+ *   its memory between calls).
  * batch*n_heads == 0 or n_patches == 0 is a successful no-op that launches
  * nothing.
  *
@@ -129,11 +136,9 @@ vattn_status vattn_forward_f16io(const uint16_t* q, const uint16_t* k, const uin
  * vattn_forward_f32q -- attention with f32 queries and f16 keys and values.
  *
  * For callers that hold k and v in f16 (computed once, attended by fresh
- * f32 queries).  It is also the attention kernel that vattn_forward runs
- * after its staging pass when 2048 < n_patches and head_dim <= 64: the
- * kernel rounds q to f16 itself (round to nearest even) once per block of
- * query rows, so the result equals vattn_forward on q and the f32 values of
- * k and v, bit for bit.
+ * f32 queries).  The kernel rounds q to f16 itself (round to nearest even)
+ * once per block of query rows, so the result equals vattn_forward on q and
+ * the f32 values of k and v, bit for bit.
  *
  * q, out: DEVICE f32 [batch, n_heads, n_patches, head_dim]; k, v: DEVICE
  *   IEEE binary16 tensors of the same shape.  q, k, v 16-byte aligned, out

@@ -78,6 +78,7 @@ enum WaitSite : uint32_t {
   kSiteDrainMma = 13,
   kSiteMmaSFree = 14,
   kSiteConvert = 16,
+  kSiteKvReady = 17,
 };
 constexpr uint32_t kStatusTimeout = 0x100u;
 
@@ -94,6 +95,12 @@ struct Params {
   int n_ktiles;   // ceil(N / kBN)
   int vec_out;    // out rows may be written with 16-byte stores
   int tma_out;    // write out through tm_o (TMA stores; head_dim <= 64, % 4 == 0)
+  // kInStageKV only: the f16 copies [B*H, N, d_pad] of k and v that the
+  // kernel writes (from the f32 maps tm_kl / tm_vl) and tm_k / tm_v read,
+  // and one ready flag per (bh, key tile), zero at launch
+  uint16_t* k16;
+  uint16_t* v16;
+  uint32_t* kv_ready;
 };
 
 // Shared-memory plan for NQ query tiles and NKB 64-column blocks of d_pad.
@@ -107,21 +114,26 @@ struct Params {
 //            slots; a fourth warpgroup rounds them to f16 into the same
 //            swizzled tiles;
 //   kInF32Q: k, v f16 copies; q f32 tiles into two slots (one per query
-//            tile), rounded to f16 by warp 3 once per work tile.
-constexpr int kInF16 = 0, kInF32 = 1, kInF32Q = 2;
+//            tile), rounded to f16 by warp 3 once per work tile;
+//   kInStageKV: as kInF32Q, and a fourth warpgroup writes the f16 copies of
+//            k and v itself (global to global, each key tile once, ahead of
+//            the blocks that read it, which wait for its ready flag).
+constexpr int kInF16 = 0, kInF32 = 1, kInF32Q = 2, kInStageKV = 3;
 
 template <int NQ, int NKB, bool kAcc = false, int kIn = kInF16>
 struct Plan {
-  static constexpr bool kF32 = kIn == kInF32;    // every operand from f32
-  static constexpr bool kF32Q = kIn == kInF32Q;  // q from f32
+  static constexpr bool kF32 = kIn == kInF32;                         // every operand from f32
+  static constexpr bool kStageKV = kIn == kInStageKV;                 // k, v copies written here
+  static constexpr bool kF32Q = kIn == kInF32Q || kIn == kInStageKV;  // q from f32
+  static constexpr bool kConvWG = kF32 || kStageKV;                   // a fourth warpgroup
   // control warpgroup + one softmax warpgroup per query tile (+ converters)
-  static constexpr int kThreads = 128 * (1 + NQ) + (kF32 ? 128 : 0);
+  static constexpr int kThreads = 128 * (1 + NQ) + (kConvWG ? 128 : 0);
   static constexpr int kTileF16 = NKB * kBoxBytes;
   static constexpr int kParts = kAcc ? 2 : 1;      // f16 terms per operand
   static constexpr int kPartBytes = kTileF16;      // offset of lo after hi
   static constexpr int kStageStride = kParts * kTileF16;
   static constexpr int kStages =  // K and V stages
-      kF32 ? 2 : (kF32Q ? 3 : (kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3))));
+      kF32 ? 2 : (kStageKV ? 2 : (kF32Q ? 3 : (kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3)))));
   // two query tiles with head_dim > 64: O needs 2 x 80..128 TMEM columns, so
   // the two tiles take turns with one P buffer
   static constexpr bool kSharedP = NQ == 2 && NKB == 2;
@@ -132,7 +144,9 @@ struct Plan {
   // 2 KB buffers (32 rows x 16 f32, 64-byte swizzle) per softmax warp
   static constexpr int kEpiBytes = (NKB == 1 && !kAcc) ? 4 * NQ * 4096 : 0;
   static constexpr int kOffEpi = kOffV + kStages * kStageStride;
-  static constexpr int kF32Slots = kF32 ? 3 : (kF32Q ? NQ : 0);
+  // f32 slots: the kInF32 ring; one per query tile for kInF32Q; and for
+  // kInStageKV one more, slot NQ, for the k / v tiles being staged
+  static constexpr int kF32Slots = kF32 ? 3 : (kStageKV ? NQ + 1 : (kF32Q ? NQ : 0));
   static constexpr int kF32TileBytes = kBM * 64 * 4;  // 128 rows x 64 f32, unswizzled
   static constexpr int kOffF32 = kOffEpi + kEpiBytes;
   static constexpr int kOffBar = kOffF32 + kF32Slots * kF32TileBytes;
@@ -143,9 +157,9 @@ struct Plan {
   // With the converter warpgroup: 65536 / 512 -> 128 per thread,
   // 2 * 40 + 2 * 216 <= 4 * 128.
   static constexpr bool kSplitRegs = NQ == 2;
-  static constexpr uint32_t kRegsSoftmax = kF32 ? 216 : 224;
-  static constexpr uint32_t kRegsOther = kF32 ? 40 : 56;
-  static constexpr uint32_t kRegsLaunch = kF32 ? 128 : 168;
+  static constexpr uint32_t kRegsSoftmax = kConvWG ? 216 : 224;
+  static constexpr uint32_t kRegsOther = kConvWG ? 40 : 56;
+  static constexpr uint32_t kRegsLaunch = kConvWG ? 128 : 168;
   // TMEM columns: S buffers at 0 and 128, P at 256 (kAcc: P lo at 320), O
   // after them; two query tiles keep their P (and O) blocks kColPStride
   // (kColOStride) apart.  Shared P (two query tiles, head_dim > 64): one P
@@ -155,7 +169,7 @@ struct Plan {
   static constexpr uint32_t kColO = kSharedP ? 320 : ((NQ == 2 || kAcc) ? 384 : 320);
   static constexpr uint32_t kColPStride = kSharedP ? 0 : 64;
   static constexpr uint32_t kColOStride = kSharedP ? 96 : 64;
-  static_assert(!kSplitRegs || (kF32 ? 2 : 1) * kRegsOther + NQ * kRegsSoftmax <=
+  static_assert(!kSplitRegs || (kConvWG ? 2 : 1) * kRegsOther + NQ * kRegsSoftmax <=
                                     static_cast<uint32_t>(kThreads / 128) * kRegsLaunch,
                 "register split too large");
   static_assert(kIn == kInF16 || (NQ == 2 && NKB == 1 && !kAcc),
@@ -187,7 +201,8 @@ enum Bar : int {
 };
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
 constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
-static_assert(kAbortOff + 4 <= 512, "barrier block overflow");
+constexpr int kConvOkOff = kAbortOff + 4;    // u32: kInStageKV slot wait result, for the warpgroup
+static_assert(kConvOkOff + 4 <= 512, "barrier block overflow");
 
 struct Waiter {
   volatile uint32_t* abort_flag;
@@ -199,6 +214,25 @@ struct Waiter {
     for (uint32_t it = 1;; ++it) {
       if (ptx::mbar_try_wait(bar, parity)) return true;
       if ((it & 31u) == 0) {
+        if (*abort_flag) return false;
+        if (ptx::global_timer_ns() - t0 > kWaitTimeoutNs) {
+          *abort_flag = 1;
+          atomicOr(&g_vattn_status, kStatusTimeout | site);
+          return false;
+        }
+      }
+    }
+  }
+
+  // Bounded wait for a flag in global memory that another block sets
+  // (release) once what it guards is written; acquire on success.
+  __device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t site) const {
+    if (ptx::ld_acquire_gpu(f) != 0) return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+      __nanosleep(64);
+      if (ptx::ld_acquire_gpu(f) != 0) return true;
+      if ((it & 15u) == 0) {
         if (*abort_flag) return false;
         if (ptx::global_timer_ns() - t0 > kWaitTimeoutNs) {
           *abort_flag = 1;
@@ -341,8 +375,100 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
   const uint32_t tile_bytes = static_cast<uint32_t>(P::kTileF16);
 
   const bool softmax_wg = warp >= 4 && warp < 4 + 4 * NQ;
-  const bool convert_wg = kF32 && warp >= 4 + 4 * NQ;
-  if (convert_wg) {
+  const bool convert_wg = P::kConvWG && warp >= 4 + 4 * NQ;
+  if (P::kStageKV && convert_wg) {
+    if (P::kSplitRegs) ptx::regs_decrease<P::kRegsOther>();
+    // ------------------------------------------- k, v staging, in the kernel
+    // Job s = one key tile (bh, j) of k and v: its rows come by TMA as f32
+    // [128 x 64] into f32 slot NQ (tm_kl / tm_vl: f32 maps, columns past
+    // head_dim and rows past N read as zero), are rounded to f16 rows of d_pad
+    // columns into the copies that tm_k / tm_v read (rows < N only), and
+    // kv_ready[bh * T + j] is set (release).  Block b takes jobs b,
+    // b + gridDim.x, ... of a sequence ordered by when they are needed: the
+    // heads whose first work tile falls in round r (work tiles r * gridDim.x
+    // .. (r + 1) * gridDim.x - 1) come before those of round r + 1, and
+    // within a round key tile j of all of them before key tile j + 1.
+    // Thread c of the 128 handles 8-column chunks c, c + 128, ... of a tile.
+    const int tid = static_cast<int>(threadIdx.x) - 128 * (1 + NQ);
+    const int dp = p.d_pad;
+    const int cpr = dp >> 3;  // 8-column chunks per f16 row
+    const int64_t n_bh = p.n_tiles / p.n_qblocks;
+    const int64_t n_jobs = n_bh * T;
+    const int64_t grid = gridDim.x;
+    const int64_t nqb = p.n_qblocks;
+    const uint32_t slot = base_s + P::kOffF32 + static_cast<uint32_t>(NQ * P::kF32TileBytes);
+    const uint32_t slot_bar = bar(kBarF32Full + NQ);
+    if (tid == 0) {
+      ptx::prefetch_tensormap(&tm_kl);
+      ptx::prefetch_tensormap(&tm_vl);
+    }
+    // Thread 0 issues each load and waits for it (bounded); the warpgroup
+    // learns the outcome through shared memory after a barrier, so that all
+    // 128 threads take the same branch and every warpgroup barrier is
+    // complete, then each thread acquires the (completed) phase itself.
+    volatile uint32_t* conv_ok = reinterpret_cast<volatile uint32_t*>(base + P::kOffBar + kConvOkOff);
+    uint32_t loads = 0;  // TMA loads into the slot (thread 0 issues them; phase = loads & 1)
+    bool ok = true;
+    auto stage = [&](const CUtensorMap* tm, uint16_t* dst, int64_t h, int64_t j, int nr) -> bool {
+      const uint32_t phase = loads & 1u;
+      ++loads;
+      if (tid == 0) {
+        ptx::mbar_arrive_expect_tx(slot_bar, P::kF32TileBytes);
+        ptx::tma_load_3d(slot, tm, slot_bar, 0, static_cast<int>(j) * kBN, static_cast<int>(h));
+        *conv_ok = w.wait(slot_bar, phase, kSiteConvert) ? 1u : 0u;
+      }
+      ptx::named_barrier_sync(1, 128);
+      if (*conv_ok == 0u) return false;
+      ptx::mbar_try_wait(slot_bar, phase);  // complete: returns at once, with acquire
+      const int chunks = nr * cpr;
+      uint16_t* row0 = dst + (h * N + j * kBN) * dp;
+      for (int c = tid; c < chunks; c += 128) {
+        const int row = c / cpr;
+        const int ch = c - row * cpr;
+        const uint32_t a = slot + static_cast<uint32_t>(row * 256 + ch * 32);
+        const float4 lo = ptx::ld_shared_v4(a);
+        const float4 hi = ptx::ld_shared_v4(a + 16u);
+        ptx::st_global_v4(row0 + static_cast<int64_t>(row) * dp + ch * 8,
+                          ptx::pack_half2(lo.x, lo.y), ptx::pack_half2(lo.z, lo.w),
+                          ptx::pack_half2(hi.x, hi.y), ptx::pack_half2(hi.z, hi.w));
+      }
+      // every thread has read the slot before the next TMA load refills it
+      ptx::fence_proxy_async_smem();
+      ptx::named_barrier_sync(1, 128);
+      return true;
+    };
+    for (int64_t s = blockIdx.x; ok && s < n_jobs; s += grid) {
+      // (bh, j) of job s
+      int64_t base_job = 0, h = 0, j = 0;
+      for (int64_t r = 0;; ++r) {
+        const int64_t h0 = (r * grid + nqb - 1) / nqb;
+        int64_t h1 = ((r + 1) * grid + nqb - 1) / nqb;
+        if (h1 > n_bh) h1 = n_bh;
+        const int64_t cnt = (h1 - h0) * T;
+        if (s < base_job + cnt) {
+          const int64_t o = s - base_job;
+          j = o / (h1 - h0);
+          h = h0 + (o - j * (h1 - h0));
+          break;
+        }
+        base_job += cnt;
+      }
+      const int nr = (N - static_cast<int>(j) * kBN) < kBN ? (N - static_cast<int>(j) * kBN) : kBN;
+      if (!(ok = stage(&tm_kl, p.k16, h, j, nr))) break;
+      if (!(ok = stage(&tm_vl, p.v16, h, j, nr))) break;
+      // the copies are read by other blocks through TMA: generic writes,
+      // then the proxy fence, the warpgroup barrier and one release
+      ptx::fence_proxy_async_global();
+      ptx::named_barrier_sync(1, 128);
+      if (tid == 0) {
+        __threadfence();
+        ptx::st_release_gpu(p.kv_ready + h * T + j, 1u);
+      }
+    }
+    // a load still in flight (after an abort) must land before the block exits
+    if (tid == 0 && loads > 0) w.drain(slot_bar, (loads - 1) & 1u, kSiteDrainTma);
+    (void)ok;
+  } else if (convert_wg) {
     if (P::kSplitRegs) ptx::regs_decrease<P::kRegsOther>();
     // ------------------------------------------------ f32 -> f16 converters
     // Ring tile n (slot n % 2) is the n-th of the sequence warp 0 loads; it
@@ -453,6 +579,13 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
             const int64_t g = static_cast<int64_t>(i) * T + j;
             const int st = kv_stage(g);
             const uint32_t free_par = kv_phase(g) ^ 1u;
+            if constexpr (P::kStageKV) {
+              // the f16 copies of this key tile are written by a block of
+              // this grid: wait for its flag, then read them with TMA
+              if (!(ok = w.wait_flag(p.kv_ready + static_cast<int64_t>(bh) * T + j, kSiteKvReady)))
+                break;
+              ptx::fence_proxy_async_global();
+            }
             if (!(ok = w.wait(bar(kBarKEmpty + st), free_par, kSiteProducerK))) break;
             ptx::mbar_arrive_expect_tx(bar(kBarKFull + st), P::kParts * tile_bytes);
             for (int kb = 0; kb < NKB; ++kb) {

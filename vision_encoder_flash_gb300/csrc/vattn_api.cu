@@ -220,15 +220,22 @@ vattn_status launch_attention_maps(const CUtensorMap& tq, const CUtensorMap& tk,
   }
   // programmatic launch: the block prologue (barriers, TMEM, tensor maps)
   // overlaps the end of the previous kernel; the producers wait for it
-  // (griddepcontrol.wait) before their first load
+  // (griddepcontrol.wait) before their first load.  kInStageKV: blocks wait
+  // for flags that other blocks of the grid set, so the grid is launched
+  // cooperatively (all blocks resident together; one per multiprocessor)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(P::kThreads);
   cfg.dynamicSmemBytes = P::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if constexpr (kIn == vattn::kInStageKV) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, tql, tkl, tvl, p);
@@ -494,9 +501,15 @@ vattn_status launch_conv1d4(const vattn::Conv1dArgs& a, int device, int sms, cud
 // attention kernel.  With two query tiles of head_dim <= 64 the attention
 // kernel reads q in f32 and rounds it itself (q is read once per work tile,
 // so that costs it little) and the staging kernel rounds k and v alone.
+// single_kernel: the k and v staging may run inside the attention kernel
+// (a cooperative launch); vattn_forward_host passes false: with it, its
+// chunked calls measured 12 % slower end to end (1.55 against 1.37 ms at
+// 8 x 16 heads, 2304 patches), where the copies, not the kernels, set the
+// time.
 // Arguments are valid (checked by the entry points).
 vattn_status run_forward(const float* q, const float* k, const float* v, float* out, int64_t bh,
-                         int N, int D, void* ws, size_t region, cudaStream_t stream, int device) {
+                         int N, int D, void* ws, size_t region, cudaStream_t stream, int device,
+                         bool single_kernel = true) {
   if (f32_direct(q, k, v, N, D)) return launch_f32_direct(q, k, v, out, bh, N, D, stream, device);
   const int d_pad = (D + 15) & ~15;
   const int nkb = d_pad <= 64 ? 1 : 2;
@@ -514,6 +527,8 @@ vattn_status run_forward(const float* q, const float* k, const float* v, float* 
   p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
   p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
   const bool q_f32 = nkb == 1 && nq == 2 && D % 4 == 0 && (reinterpret_cast<uintptr_t>(q) & 15u) == 0;
+  const bool kv_in_kernel = single_kernel && q_f32 &&
+                            ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
   __half* q16 = static_cast<__half*>(ws);
   __half* k16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + region);
   __half* v16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + 2 * region);
@@ -523,6 +538,24 @@ vattn_status run_forward(const float* q, const float* k, const float* v, float* 
     return st;
   if ((st = make_tmap16(&tk, k16, bh, N, d_pad)) != VATTN_OK) return st;
   if ((st = make_tmap16(&tv, v16, bh, N, d_pad)) != VATTN_OK) return st;
+  if (kv_in_kernel) {
+    // one kernel: it writes the f16 copies of k and v itself, each key tile
+    // once, and the blocks that read a tile wait for its ready flag (the
+    // flags sit in the region of the q copy, which this path does not use)
+    uint32_t* flags = reinterpret_cast<uint32_t*>(q16);
+    const size_t flag_bytes = static_cast<size_t>(bh) * p.n_ktiles * sizeof(uint32_t);
+    const cudaError_t e = cudaMemsetAsync(flags, 0, flag_bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the key-tile flags");
+    p.k16 = reinterpret_cast<uint16_t*>(k16);
+    p.v16 = reinterpret_cast<uint16_t*>(v16);
+    p.kv_ready = flags;
+    CUtensorMap tk32, tv32;  // the f32 tiles the kernel stages from
+    vattn_status sm;
+    if ((sm = make_tmap32(&tk32, k, bh, N, D)) != VATTN_OK) return sm;
+    if ((sm = make_tmap32(&tv32, v, bh, N, D)) != VATTN_OK) return sm;
+    return launch_attention_maps<2, 1, false, false, vattn::kInStageKV>(
+        tq, tk, tv, tq, tk32, tv32, p, static_cast<unsigned>(grid), stream, device);
+  }
   const int64_t rows = bh * N;
   const uintptr_t src_or = (q_f32 ? 0u : reinterpret_cast<uintptr_t>(q)) |
                            reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v);
@@ -1088,7 +1121,7 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
       if (!ck(cudaStreamWaitEvent(s_comp, ev_in[c], 0), "cudaStreamWaitEvent")) break;
       if (c >= 2 && !ck(cudaStreamWaitEvent(s_comp, ev_out[c - 2], 0), "cudaStreamWaitEvent")) break;
       st = run_forward(in_ptr(c, 0), in_ptr(c, 1), in_ptr(c, 2), out_ptr(c), hn, N, D, ws16,
-                       static_cast<size_t>(region), s_comp, device);
+                       static_cast<size_t>(region), s_comp, device, false);
       if (st != VATTN_OK || !ck(cudaEventRecord(ev_comp[c], s_comp), "cudaEventRecord")) break;
       // copy out
       if (!ck(cudaStreamWaitEvent(s_out, ev_comp[c], 0), "cudaStreamWaitEvent") ||
