@@ -266,10 +266,12 @@ vattn_status vattn_conv1d_step(const float* input, float* buffer, const float* w
  *
  * The heads (batch * n_heads) are cut into up to eight chunks of whole heads.
  * Three streams the library keeps per device carry, for each chunk, the
- * host-to-device copies of its q, k and v, the two kernels of vattn_forward,
- * and the device-to-host copy of its output, so that the copies of one chunk
- * overlap the kernels of the next.  The result is bit-identical to
- * vattn_forward on the same values (the same kernels per head).
+ * host-to-device copies of its q, k and v, the kernels of vattn_forward (the
+ * direct f32 kernel, else the staging kernel and the attention kernel: not
+ * the single cooperative kernel), and the device-to-host copy of its output,
+ * so that the copies of one chunk overlap the kernels of the next.  The
+ * result is bit-identical to vattn_forward on the same values (the same
+ * rounding and arithmetic per head).
  *
  * q, k, v, out: HOST pointers to contiguous f32 [batch, n_heads, n_patches,
  *   head_dim], head-major, 4-byte aligned; out must not overlap q, k or v.

@@ -6,13 +6,21 @@
 // (rullama 0.1.0): q/k/v rounded to f16, scores and P.V accumulated in f32,
 // f32 online softmax with running (m, l, o), no 1/sqrt(head_dim) factor.
 //
-// Inputs are the f16 copies written by vattn_stage_kernel (stage_kernel.cuh):
-// [B*H, N, d_pad] f16, d_pad = head_dim rounded up to 16, zero padding --
-// or, in the kF32 variant (two query tiles, head_dim <= 64), the caller's f32
-// tensors: TMA brings f32 tiles into a ring of shared-memory slots and a
-// fourth warpgroup rounds them to f16 into the same swizzled operand tiles,
-// with the staging kernel's rounding (round to nearest even), so both paths
-// give bit-identical results.
+// Operands (input mode kIn; every mode rounds f32 to f16 to nearest even,
+// as the staging kernel does, so all give bit-identical results):
+//   kInF16     the f16 copies written by vattn_stage_kernel
+//              (stage_kernel.cuh), [B*H, N, d_pad] f16, d_pad = head_dim
+//              rounded up to 16, zero padding, by TMA;
+//   kInF32     (two query tiles, head_dim <= 64) the caller's f32 tensors:
+//              TMA brings f32 tiles into a ring of shared-memory slots and a
+//              fourth warpgroup rounds them into the swizzled operand tiles;
+//   kInF32Q    k, v as kInF16; q in f32, rounded by warp 3 once per work
+//              tile;
+//   kInStageKV q as kInF32Q; a fourth warpgroup writes the f16 copies of k
+//              and v itself (each key tile once, by one block of the
+//              cooperative grid, which then sets the tile's ready flag), and
+//              the K/V producer of every block waits for a tile's flag
+//              before reading it by TMA as in kInF16.
 // The shader's design (8 queries x 32 keys per 64-thread workgroup, scalar
 // dot products, subgroup reductions) is replaced by a GB300 one:
 //   * a work tile = one bh and NQ query tiles of 128 rows; the grid is one
@@ -36,7 +44,11 @@
 //   * the same warpgroup divides by l and stores its rows of out (f32);
 //   * the producers wait for the previous kernel (griddepcontrol.wait)
 //     before their first load, so with a programmatic launch the block
-//     prologue overlaps the end of the staging pass.
+//     prologue overlaps the end of the staging pass;
+//   * 384 threads (control warpgroup + two softmax warpgroups), or 512 with
+//     the fourth warpgroup of kInF32 / kInStageKV; setmaxnreg gives the
+//     softmax warps 224 (216 with 512 threads) registers and the others 56
+//     (40).
 // TMEM columns (512): S buffers [0,128) and [128,256); with two query tiles
 // P0, P1 at 256, 320 and O0, O1 at 384, 448 (head_dim <= 64), or one P
 // buffer at 256 that the two tiles take in turn and O0, O1 at 320, 416
