@@ -331,14 +331,16 @@ def run_gpu_offsets(torch_dev, q, k, v, offsets):
     return out[4:4 + numel].cpu().numpy().reshape(q.shape)
 
 
-# Two-pass shapes whose attention kernel rounds q itself (two query tiles,
-# head_dim <= 64 and a multiple of 4, q 16-byte aligned, past the direct
-# path's 2048 patches): the staging kernel rounds k and v only.
-Q_F32 = [(1, 2, 2049, 64), (1, 2, 2300, 36), (1, 3, 2500, 20), (2, 40, 2176, 64)]
+# Shapes past the direct path's 2048 patches with head_dim <= 64 and a
+# multiple of 4 (and head_dim 20 from 129 patches): with q, k, v 16-byte
+# aligned, one cooperative kernel that writes the f16 copies of k and v
+# itself and rounds q; ragged last key tiles, a grid smaller than the GPU
+# (2 heads) and several rounds of work tiles per block (80 heads).
+STAGED = [(1, 2, 2049, 64), (1, 2, 2300, 36), (1, 3, 2500, 20), (2, 40, 2176, 64)]
 
 
-@pytest.mark.parametrize("shape", Q_F32)
-def test_query_f32_path(torch_dev, shape):
+@pytest.mark.parametrize("shape", STAGED)
+def test_single_kernel_staging_path(torch_dev, shape):
     q, k, v = make_inputs(*shape, seed=5300 + shape[2] + shape[3])
     got = run_gpu(torch_dev, q, k, v)
     b, h, n, d = shape
@@ -352,10 +354,14 @@ def test_query_f32_path(torch_dev, shape):
 
 
 @pytest.mark.parametrize("shape", [(1, 2, 2049, 64), (2, 40, 2176, 64), (1, 3, 2500, 20)])
-def test_query_f32_and_staged_query_agree_bitwise(torch_dev, shape):
-    # q 16-byte aligned: the attention kernel rounds q; q 4-byte aligned only:
-    # the staging kernel does.  The same rounding either way: identical bits.
+def test_single_kernel_and_two_kernel_modes_agree_bitwise(torch_dev, shape):
+    # all 16-byte aligned: the single kernel (k, v staged inside, q rounded
+    # in it); q 4-byte aligned only: staging of q, k, v then the attention
+    # kernel; k 4-byte aligned only: staging of k, v then the attention
+    # kernel that rounds q.  The same rounding every way: identical bits.
     q, k, v = make_inputs(*shape, seed=5400 + shape[2])
     a = run_gpu_offsets(torch_dev, q, k, v, (4, 4, 4))
     b = run_gpu_offsets(torch_dev, q, k, v, (1, 4, 4))
+    c = run_gpu_offsets(torch_dev, q, k, v, (4, 1, 4))
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert np.array_equal(a.view(np.uint32), c.view(np.uint32))
