@@ -186,6 +186,78 @@ def gpu_smi_id(torch, dev) -> str:
     return str(dev.index)
 
 
+def gpu_numa_node(torch, dev):
+    """NUMA node of the GPU's PCI function (sysfs), or None."""
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    dom = getattr(props, "pci_domain_id", None)
+    pdev = getattr(props, "pci_device_id", None)
+    if bus is None or dom is None or pdev is None:
+        return None
+    try:
+        with open(f"/sys/bus/pci/devices/{dom:04x}:{bus:02x}:{pdev:02x}.0/numa_node") as f:
+            node = int(f.read().strip())
+    except (OSError, ValueError):
+        return None
+    return node if node >= 0 else None
+
+
+def node_cpus(node):
+    """CPUs of a NUMA node (sysfs cpulist), as a set; empty if unknown."""
+    cpus = set()
+    try:
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            text = f.read().strip()
+    except OSError:
+        return cpus
+    for part in text.split(","):
+        if not part:
+            continue
+        a, _, b = part.partition("-")
+        cpus.update(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def copy_ceiling(torch, dev, nbytes=256 * 1024 * 1024, reps=5):
+    """Pinned host <-> device copy rates (GB/s, best of `reps`): host to
+    device alone, device to host alone, and both at once on two streams
+    (one cudaMemcpyAsync each way)."""
+    n = nbytes // 4
+    h_in = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    h_out = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    h_in.fill_(1.0)
+    d_a = torch.empty(n, dtype=torch.float32, device=dev)
+    d_b = torch.empty(n, dtype=torch.float32, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            best = min(best, time.perf_counter() - t)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_b, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_h2d, t_d2h, t_both = timed(h2d), timed(d2h), timed(both)
+    del h_in, h_out, d_a, d_b
+    return {"h2d_gbs": round(nbytes / t_h2d / 1e9, 1), "d2h_gbs": round(nbytes / t_d2h / 1e9, 1),
+            "both_gbs": round(2 * nbytes / t_both / 1e9, 1), "bytes_each_way": nbytes}
+
+
 # ---------------------------------------------------------------- oracle timing
 def oracle_rate(workload, q, k, v, target_s: float, max_rows=None):
     """Time the oracle on a bounded sample of query rows; returns
@@ -209,6 +281,30 @@ def oracle_rate(workload, q, k, v, target_s: float, max_rows=None):
     dt = time.perf_counter() - t
     flops = 4.0 * n_rows * workload.n_patches * workload.head_dim
     return flops / dt / 1e12, dt, n_rows, threads
+
+
+def oracle_seconds(w, q, k, v, threads, target_s=3.0):
+    """Seconds the oracle takes for the whole workload w on `threads`
+    threads: timed in full when that is short, else on a random sample of
+    query rows (each over all keys) scaled to the full row count."""
+    import numpy as np
+
+    import oracle
+    total = q.shape[0] * q.shape[1] * q.shape[2]
+    rng = np.random.Generator(np.random.PCG64(w.seed + 7))
+    probe = min(total, max(threads, 16))
+    t = time.perf_counter()
+    oracle.rows(q, k, v, rng.integers(0, total, size=probe), threads=threads)
+    per_row = (time.perf_counter() - t) / probe
+    if per_row * total <= target_s:
+        t = time.perf_counter()
+        oracle.forward(q, k, v, threads=threads)
+        return time.perf_counter() - t, "whole workload"
+    n_rows = int(max(threads, min(total, target_s / max(per_row, 1e-9))))
+    t = time.perf_counter()
+    oracle.rows(q, k, v, rng.integers(0, total, size=n_rows), threads=threads)
+    dt = time.perf_counter() - t
+    return dt * total / n_rows, f"{n_rows} random rows of {total}, scaled to all rows"
 
 
 # ---------------------------------------------------------------- arms
@@ -375,20 +471,56 @@ def run_vattn(args, workload):
     pk, pk_src = peaks()
     peak_tf = float(pk["bf16_tflops"]) * F16_OVER_BF16_NOMINAL
 
-    # ---- end to end through the public API: pinned host tensors in, host out
-    e2e_steps = max(3, min(args.steps, 30))
-    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
-    oh = torch.empty(q.shape, dtype=torch.float32, pin_memory=True)
-    vef.forward(qh, kh, vh, out=oh)  # warm the allocator
-    barrier()
-    torch.cuda.synchronize(dev)
-    t = time.perf_counter()
-    for _ in range(e2e_steps):
-        vef.forward(qh, kh, vh, out=oh)  # H2D copies, kernel, D2H copy, stream sync
-    e2e_s = max_over_ranks((time.perf_counter() - t) / e2e_steps, pg, dev)
-    e2e_value = weak_scaling_value(flops, world, e2e_s * 1e3)
-    h2d = 3 * q.nbytes
-    d2h = oh.numel() * 4
+    # ---- end to end through the public API: pinned host tensors in, host out.
+    # The pinned buffers are allocated (and first touched) by this thread
+    # while it runs on the CPUs of the GPU's own NUMA node, so their pages sit
+    # in the host memory nearest the GPU; the plain copy rates of that memory
+    # (one 256 MB cudaMemcpyAsync each way, alone and both at once) are the
+    # ceiling the end-to-end leg is judged against.
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 30))
+        numa = gpu_numa_node(torch, dev)
+        cpus = node_cpus(numa) if numa is not None else set()
+        old_aff = None
+        bound_node = None
+        if cpus and hasattr(os, "sched_setaffinity"):
+            old_aff = os.sched_getaffinity(0)
+            if cpus & old_aff:
+                os.sched_setaffinity(0, cpus & old_aff)
+                bound_node = numa
+            else:
+                old_aff = None
+        qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (q, k, v))
+        oh = torch.empty(q.shape, dtype=torch.float32, pin_memory=True)
+        ceiling = copy_ceiling(torch, dev)
+        if old_aff is not None:
+            os.sched_setaffinity(0, old_aff)
+        vef.forward(qh, kh, vh, out=oh)  # warm the allocator
+        barrier()
+        torch.cuda.synchronize(dev)
+        t = time.perf_counter()
+        for _ in range(e2e_steps):
+            vef.forward(qh, kh, vh, out=oh)  # H2D copies, kernel, D2H copy, stream sync
+        e2e_s = max_over_ranks((time.perf_counter() - t) / e2e_steps, pg, dev)
+        e2e_value = weak_scaling_value(flops, world, e2e_s * 1e3)
+        h2d = 3 * q.nbytes
+        d2h = oh.numel() * 4
+        # the copies alone at the measured concurrent rate bound a step from below
+        link_s = max((h2d + d2h) / (ceiling["both_gbs"] * 1e9), h2d / (ceiling["h2d_gbs"] * 1e9))
+
+        e2e = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": e2e_s * 1e3,
+               "copy_peak_gbs": ceiling,
+               "copy_bound_ms": link_s * 1e3,
+               "frac_of_link": link_s / e2e_s,
+               "host_numa_node": bound_node,
+               "gpu_numa_node": numa,
+               "link_note": "copy_bound_ms: the step's bytes at the measured pinned copy rates "
+                            "(max of in+out at the concurrent rate and in alone at the "
+                            "host-to-device rate); frac_of_link = copy_bound_ms / ms_per_step",
+               "path": "vision_encoder_flash_gb300.forward on pinned host tensors (vattn_forward_host: eight chunks of heads, copies overlapping the kernels)"}
 
     # ---- oracle on the host cores (rank 0, N = 1 only)
     cpu_baseline = None
@@ -422,13 +554,27 @@ def run_vattn(args, workload):
             ms = a.elapsed_time(b) / reps
             cold = cold_call_ms(torch, dev, stream, lambda: vef.forward_raw(*xp))
             c10, c50, c90 = percentiles(cold)
+            wbytes = 16 * w.batch * w.n_heads * w.n_patches * w.head_dim
             extras[w.name] = {"ms": round(ms, 5), "tflops": round(w.flops / ms / 1e9, 2),
                               "frac_of_peak": round(w.flops / ms / 1e9 / peak_tf, 4),
+                              "bytes": wbytes,
+                              "achieved_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
+                              "frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4),
                               "l2": "hot (back-to-back, inputs may fit in L2)",
                               "cold_ms_p10_p50_p90": [round(c10, 5), round(c50, 5), round(c90, 5)],
                               "cold_tflops_p50": round(w.flops / c50 / 1e9, 2),
                               "cold": "L2 flushed (512 MB written) before each of 30 calls, "
                                       "outside the timed events"}
+            extras[w.name]["cold_gbs_p50"] = round(wbytes / (c50 * 1e-3) / 1e9, 1)
+            if idx <= 3 and world == 1 and not args.no_cpu_baseline:
+                # the oracle on one core and on all host cores (context)
+                import oracle
+                one_s, one_how = oracle_seconds(w, xq, xk, xv, 1)
+                all_t = oracle.default_threads()
+                all_s, all_how = oracle_seconds(w, xq, xk, xv, all_t)
+                extras[w.name].update({"oracle_1core_s": round(one_s, 4), "oracle_1core_how": one_how,
+                                       f"oracle_{all_t}core_s": round(all_s, 4),
+                                       "oracle_allcore_how": all_how})
             if w.head_dim % 8 == 0:  # the attention kernel alone (f16 inputs)
                 x16 = [t.half() for t in xs]
                 xp16 = (x16[0].data_ptr(), x16[1].data_ptr(), x16[2].data_ptr(), xo.data_ptr(),
@@ -545,9 +691,7 @@ def run_vattn(args, workload):
                          "how": "per-call time minus the attention kernel's time"}},
         "cpu_baseline": cpu_baseline,
         "clocks": clocks,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "vision_encoder_flash_gb300.forward on pinned host tensors (vattn_forward_host: eight chunks of heads, copies overlapping the kernels)"},
+        "e2e": e2e,
         "gpu_launches": (1 if one_kernel else 2) * args.steps,  # (staging +) attention per step
         "other_workloads": extras,
         "variants": variants,
@@ -628,6 +772,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=5, choices=sorted(WORKLOADS))
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (host buffers); for profiling the device steps")
     ap.add_argument("--conv1d-only", action="store_true",
                     help="time only the conv1d rolling-buffer step and print its line")
     args = ap.parse_args(argv)

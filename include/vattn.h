@@ -300,6 +300,14 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
 #define VATTN_NOALLOC_MAX_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /*
+ * Size of the second fixed array of vattn_forward_noalloc: the flags a call
+ * clears at its start and the partial results of tiles that the work
+ * schedule cuts between two thread blocks (16 MiB: room for every schedule
+ * on a GPU of up to 152 multiprocessors).
+ */
+#define VATTN_NOALLOC_PART_BYTES (16u * 1024u * 1024u)
+
+/*
  * vattn_forward_noalloc -- vattn_forward without any device memory
  * allocation.  The shader this library follows has no counterpart: it is an
  * interface for callers that may not allocate while they run, such as a
@@ -308,11 +316,15 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
  * allocation's cost or a late out-of-memory failure.
  *
  * Arguments, layout, result and error codes are those of vattn_forward, and
- * so are its kernels.  The f16 copies that vattn_forward makes go to a
- * fixed array of VATTN_NOALLOC_MAX_SCRATCH_BYTES that the library's device
- * code holds on every device it is loaded on (for the life of the process),
- * instead of a pool allocation; the call makes no cudaMalloc/cudaFree-type
- * call.
+ * so are its kernels and its mode (vattn_forward_mode).  The workspace that
+ * vattn_forward takes from its pool goes to a fixed array of
+ * VATTN_NOALLOC_MAX_SCRATCH_BYTES that the library's device code holds on
+ * every device it is loaded on (for the life of the process): the f16
+ * copies of q, k and v in the two-kernel mode; the f16 copies of k and v,
+ * written by the attention kernel itself, and one ready flag per (head, key
+ * tile) in the single cooperative kernel's mode.  The call makes no
+ * cudaMalloc/cudaFree-type call; the flags are cleared by a memset on
+ * `stream` at the start of each call.
  *
  * Limit: a problem whose f16 copies (3 x 256-byte-rounded
  * batch*n_heads*n_patches*round_up(head_dim, 16)*2 bytes) exceed the array is
@@ -324,14 +336,101 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
  * first call outside any stream capture.
  *
  * Calls that can overlap in time on one device -- on different streams, or
- * from several host threads -- share the one array and race: their results
- * are undefined.  Order them (one stream, or events) or use vattn_forward.
- * Nothing in the array needs to start at zero; each call writes what it
- * reads.
+ * from several host threads -- share the one array and race, on the f16
+ * copies and on the ready flags: their results are undefined (a flag that
+ * another call clears can also make a wait run out, which ends in
+ * VATTN_ERR_DEVICE_TIMEOUT from vattn_device_status, not in a hang).
+ * Order them (one stream, or events) or use vattn_forward.  Apart from the
+ * flags, which each call clears, nothing in the array needs to start at
+ * zero: each call writes what it reads.
  */
 vattn_status vattn_forward_noalloc(const float* q, const float* k, const float* v, float* out,
                                    int64_t batch, int64_t n_heads, int64_t n_patches,
                                    int64_t head_dim, void* stream);
+
+/*
+ * Kernel modes of vattn_forward (all give bit-identical results: the same
+ * f16 rounding and the same tensor-core arithmetic).  The shader has one
+ * compute pass per call; these are this library's ways of scheduling it.
+ *   VATTN_MODE_NONE           empty problem: nothing is launched;
+ *   VATTN_MODE_DIRECT         one kernel on the f32 tiles (q, k, v rounded
+ *                             to f16 in shared memory), no workspace;
+ *   VATTN_MODE_SINGLE_KERNEL  a memset of key-tile flags and one cooperative
+ *                             kernel that writes the f16 copies of k and v
+ *                             itself while it computes;
+ *   VATTN_MODE_TWO_KERNELS    the f16 staging kernel, then the attention
+ *                             kernel.
+ */
+typedef enum {
+  VATTN_MODE_NONE = 0,
+  VATTN_MODE_DIRECT = 1,
+  VATTN_MODE_SINGLE_KERNEL = 2,
+  VATTN_MODE_TWO_KERNELS = 3
+} vattn_mode;
+
+/*
+ * vattn_forward_mode -- the mode (vattn_mode) that vattn_forward takes, on
+ * the current device, for exactly these arguments.  Checks the arguments
+ * as vattn_forward does (same error codes, on the host) and launches
+ * nothing.  The first query on a device that could take the single
+ * cooperative kernel reads the device's cooperative-launch support and the
+ * kernel's occupancy (CUDA calls; cached per device).  vattn_forward_noalloc
+ * takes the same mode; vattn_forward_host never takes the single kernel.
+ * The shader has no counterpart: this exists for callers that plan memory
+ * or launches, and for tests.
+ */
+vattn_status vattn_forward_mode(const float* q, const float* k, const float* v, const float* out,
+                                int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, int* mode);
+
+/*
+ * vattn_forward_mode_for -- the rule behind vattn_forward_mode, with the
+ * device facts passed in instead of read from a device: aligned = q, k and
+ * v are all 16-byte aligned; cooperative_launch = the device attribute
+ * cudaDevAttrCooperativeLaunch; blocks_per_sm = resident blocks per
+ * multiprocessor of the single cooperative kernel (0 when it does not fit).
+ * The single kernel is taken only when cooperative_launch != 0,
+ * blocks_per_sm >= 1 and vattn_set_single_kernel has not forbidden it.
+ * Pure host function (no CUDA call).  Sizes are checked as in
+ * vattn_forward; *mode = VATTN_MODE_NONE for an empty problem.
+ */
+vattn_status vattn_forward_mode_for(int64_t batch, int64_t n_heads, int64_t n_patches,
+                                    int64_t head_dim, int aligned, int cooperative_launch,
+                                    int blocks_per_sm, int* mode);
+
+/*
+ * vattn_set_single_kernel -- allow (allow != 0, the default) or forbid
+ * (allow == 0) the single cooperative kernel, process-wide.  Forbidden, the
+ * calls that would take it take VATTN_MODE_TWO_KERNELS instead (same
+ * result, one more kernel); useful where cooperative grids are not wanted,
+ * for example on a GPU shared under MPS with a limit on multiprocessors.
+ * (Without the switch, a cooperative launch that the driver refuses as too
+ * large also falls back to the two kernels.)  Returns the previous setting
+ * (1 or 0).  Not synchronised with calls in flight on other host threads:
+ * set it before them.
+ */
+int vattn_set_single_kernel(int allow);
+
+/*
+ * vattn_set_split_tiles -- allow (allow != 0) or forbid (allow == 0, the
+ * default) cut work tiles, process-wide.  The attention kernel is
+ * persistent (one thread block per multiprocessor); when the work tiles
+ * (128 or 256 query rows of one head) do not divide evenly over the blocks,
+ * vattn_forward and vattn_forward_noalloc cut the tiles of the last round by
+ * key range, one equal share per block, and the two parts of a cut tile are
+ * combined by the log-sum-exp rule (the shader's rescale of (m, l, o)).  The
+ * result is the same attention, but the rounding of a cut tile's rows then
+ * depends on how the call's work was shared out, i.e. on the other heads in
+ * the call.  Forbidden, every tile runs whole in one block: each output row
+ * depends only on its own head's inputs (bit-identical whatever else the
+ * call holds, as in vattn_forward_f16 / _f32q / _host, which never cut),
+ * at the price of a partial last round.  Measured on GB300, the pieces'
+ * extra prologues and merges cost about what the balanced round saves, so
+ * cut tiles are off unless allowed here.  Returns the previous setting.  Not
+ * synchronised with calls in flight on other host threads: set it before
+ * them.  The shader has no counterpart (one workgroup per block of rows).
+ */
+int vattn_set_split_tiles(int allow);
 
 /*
  * vattn_device_status -- reads and clears the kernel-side error word of the

@@ -1,0 +1,79 @@
+"""The rule that picks vattn_forward's kernel mode, run on the host with the
+device facts passed in (vattn_forward_mode_for: no GPU needed).
+
+The single cooperative kernel (k and v staged inside it) is taken only where
+the device supports cooperative launches and holds one of its blocks per
+multiprocessor; any device that does not falls back to the two-kernel mode,
+which gives the same bits.  The process-wide switch vattn_set_single_kernel
+forbids the single kernel the same way."""
+import pytest
+
+import vision_encoder_flash_gb300 as vef
+from vision_encoder_flash_gb300 import _lib
+
+DIRECT, SINGLE, TWO = _lib.MODE_DIRECT, _lib.MODE_SINGLE_KERNEL, _lib.MODE_TWO_KERNELS
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from vision_encoder_flash_gb300 import build
+    build.build()
+    return vef.load_library()
+
+
+@pytest.mark.parametrize("shape,aligned,mode", [
+    ((8, 16, 2304, 64), 1, SINGLE),      # the benchmark workload
+    ((8, 16, 2304, 64), 0, TWO),         # unaligned pointers: neither one-kernel mode
+    ((4, 16, 1024, 64), 1, DIRECT),      # <= 2048 patches, head_dim 33..64
+    ((4, 16, 2048, 64), 1, DIRECT),
+    ((4, 16, 2049, 64), 1, SINGLE),
+    ((1, 16, 4100, 72), 1, TWO),         # head_dim past 64
+    ((1, 16, 4100, 62), 1, TWO),         # head_dim not a multiple of 4
+    ((1, 2, 64, 32), 1, TWO),            # one query tile (<= 128 patches)
+    ((1, 2, 129, 32), 1, SINGLE),        # head_dim <= 32 takes the single kernel from 129 patches
+    ((1, 16, 256, 64), 1, DIRECT),
+    ((2, 2, 130, 128), 1, TWO),
+])
+def test_mode_rule_on_a_capable_device(lib, shape, aligned, mode):
+    assert _lib.forward_mode_for(*shape, aligned, 1, 1) == mode
+
+
+@pytest.mark.parametrize("coop,blocks", [(0, 1), (1, 0), (0, 0)])
+def test_single_kernel_needs_cooperative_launch_and_a_resident_block(lib, coop, blocks):
+    # where the single kernel would run, a device without the facts gets two kernels
+    assert _lib.forward_mode_for(8, 16, 2304, 64, 1, coop, blocks) == TWO
+    assert _lib.forward_mode_for(1, 2, 129, 32, 1, coop, blocks) == TWO
+    # the other modes do not depend on them
+    assert _lib.forward_mode_for(4, 16, 1024, 64, 1, coop, blocks) == DIRECT
+    assert _lib.forward_mode_for(1, 16, 4100, 72, 1, coop, blocks) == TWO
+
+
+def test_process_wide_switch(lib):
+    prev = _lib.set_single_kernel(False)
+    try:
+        assert prev is True
+        assert _lib.forward_mode_for(8, 16, 2304, 64, 1, 1, 1) == TWO
+        assert _lib.forward_mode_for(4, 16, 1024, 64, 1, 1, 1) == DIRECT
+    finally:
+        assert _lib.set_single_kernel(True) is False
+    assert _lib.forward_mode_for(8, 16, 2304, 64, 1, 1, 1) == SINGLE
+
+
+def test_empty_and_invalid(lib):
+    assert _lib.forward_mode_for(0, 16, 2304, 64, 1, 1, 1) == _lib.MODE_NONE
+    assert _lib.forward_mode_for(8, 16, 0, 64, 1, 1, 1) == _lib.MODE_NONE
+    with pytest.raises(vef.VattnError) as e:
+        _lib.forward_mode_for(8, 16, 2304, 129, 1, 1, 1)
+    assert e.value.status == 2
+    with pytest.raises(vef.VattnError) as e:
+        _lib.forward_mode_for(8, -1, 2304, 64, 1, 1, 1)
+    assert e.value.status == 1
+
+
+def test_device_query_checks_arguments_before_any_cuda_call(lib):
+    fake = 0x10000
+    with pytest.raises(vef.VattnError) as e:  # out overlaps q: rejected on the host
+        _lib.forward_mode(fake, fake, fake, fake + 4, 1, 1, 2, 4)
+    assert e.value.status == 1
+    # an empty problem needs no device either
+    assert _lib.forward_mode(fake, fake, fake, fake + 2 ** 30, 0, 1, 2, 4) == _lib.MODE_NONE

@@ -6,8 +6,12 @@ match vattn_forward's within the parity tolerance (3e-3 max abs, 1e-3 rel
 L2); with the same kernels on the same inputs it is in fact bit-identical.
 Each case makes two noalloc calls in a row, the second on other inputs and
 another shape, so that a call which read the previous call's staging would
-show.  This file is collected last and also passes run on its own in a fresh
-process: it builds and loads the library itself.
+show.  Every shape here takes a mode that stages through the fixed array
+(the single cooperative kernel, whose flags and f16 k, v copies live there,
+or the two-kernel mode, whose f16 q, k, v copies do): the direct f32 kernel
+uses no scratch, so its shapes would prove nothing, and each case asserts
+its mode.  This file is collected last and also passes run on its own in a
+fresh process: it builds and loads the library itself.
 """
 import numpy as np
 import pytest
@@ -47,6 +51,16 @@ def device_inputs(torch_dev, shape, seed):
     return tuple(torch.from_numpy(x).to(dev) for x in (q, k, v))
 
 
+SCRATCH_MODES = (_lib.MODE_SINGLE_KERNEL, _lib.MODE_TWO_KERNELS)
+
+
+def assert_stages_through_scratch(q, k, v, out):
+    b, h, n, d = q.shape
+    mode = _lib.forward_mode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), b, h, n, d)
+    assert mode in SCRATCH_MODES, f"{tuple(q.shape)} takes mode {mode}, which uses no scratch"
+    return mode
+
+
 def call(fn, q, k, v, out, stream):
     b, h, n, d = q.shape
     fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), b, h, n, d, stream.cuda_stream)
@@ -64,9 +78,14 @@ def assert_close(got, ref, what):
 
 
 @pytest.mark.parametrize("first,second", [
-    ((4, 16, 1024, 64), (1, 3, 200, 40)),      # 1024-patch batch, then a small ragged one
-    ((1, 16, 4100, 72), (2, 2, 130, 128)),     # ragged tail at head_dim 72, then head_dim 128
-    ((1, 2, 64, 32), (8, 4, 577, 64)),         # tiny, then a larger ragged one
+    # single cooperative kernel (flags + f16 k, v in the array), then two
+    # kernels on a head_dim that is not a multiple of 4 (f16 q, k, v there)
+    ((1, 16, 2304, 64), (1, 3, 200, 38)),
+    # two kernels: ragged tail at head_dim 72, then head_dim 128
+    ((1, 16, 4100, 72), (2, 2, 130, 128)),
+    # two kernels on one query tile (64 patches), then the single kernel at
+    # head_dim 20 with a ragged last key tile
+    ((1, 2, 64, 32), (2, 8, 2500, 20)),
 ])
 def test_noalloc_matches_forward_two_calls_in_a_row(torch_dev, first, second):
     torch, dev = torch_dev
@@ -76,6 +95,7 @@ def test_noalloc_matches_forward_two_calls_in_a_row(torch_dev, first, second):
     refs, outs = [], []
     for q, k, v in ins:
         ref = torch.empty_like(q)
+        assert_stages_through_scratch(q, k, v, ref)
         call(_lib.forward_raw, q, k, v, ref, stream)
         refs.append(ref)
         outs.append(torch.full_like(q, float("nan")))
@@ -98,6 +118,7 @@ def test_noalloc_largest_accepted_problem(torch_dev):
     q, k, v = device_inputs(torch_dev, shape, 903)
     stream = torch.cuda.current_stream(dev)
     ref = torch.empty_like(q)
+    assert_stages_through_scratch(q, k, v, ref)
     call(_lib.forward_raw, q, k, v, ref, stream)
     out = torch.full_like(q, float("nan"))
     call(_lib.forward_noalloc_raw, q, k, v, out, stream)
@@ -125,12 +146,15 @@ def test_noalloc_rejects_a_problem_past_the_scratch(torch_dev):
     assert torch.isfinite(out).all()
 
 
-def test_noalloc_does_not_take_device_memory(torch_dev):
+@pytest.mark.parametrize("shape", [(1, 16, 2304, 64), (1, 16, 4100, 72)])
+def test_noalloc_does_not_take_device_memory(torch_dev, shape):
     """After a first call of a shape (which loads the code it needs), further
-    calls leave the device's free memory unchanged."""
+    calls leave the device's free memory unchanged: the single cooperative
+    kernel and the two-kernel mode, both staging through the array."""
     torch, dev = torch_dev
-    q, k, v = device_inputs(torch_dev, (4, 16, 1024, 64), 904)
+    q, k, v = device_inputs(torch_dev, shape, 904)
     out = torch.empty_like(q)
+    assert_stages_through_scratch(q, k, v, out)
     stream = torch.cuda.current_stream(dev)
     call(_lib.forward_noalloc_raw, q, k, v, out, stream)
     torch.cuda.synchronize(dev)
@@ -146,3 +170,27 @@ def test_noalloc_does_not_take_device_memory(torch_dev):
 def test_noalloc_empty_problem_is_a_no_op(torch_dev):
     assert _lib.forward_noalloc_status(0, 0, 0, 0, 2, 4, 0, 64, 0) == 0
     assert _lib.forward_noalloc_status(0, 0, 0, 0, 0, 4, 10, 64, 0) == 0
+
+
+def test_noalloc_workload_against_the_oracle(torch_dev, oracle_mod):
+    """The seeded 16-head, 4100-patch, head_dim 72 workload (two kernels, its
+    f16 copies filling most of the array) through the allocation-free entry,
+    compared with the f64 oracle on every output element at the acceptance
+    bar (max abs 3e-3, rel L2 1e-3)."""
+    from vattn_inputs import workload_inputs
+    torch, dev = torch_dev
+    qn, kn, vn = workload_inputs(4)
+    q, k, v = (torch.from_numpy(x).to(dev) for x in (qn, kn, vn))
+    assert staged_bytes(*q.shape) <= SCRATCH
+    out = torch.full_like(q, float("nan"))
+    assert_stages_through_scratch(q, k, v, out)
+    stream = torch.cuda.current_stream(dev)
+    call(_lib.forward_noalloc_raw, q, k, v, out, stream)
+    torch.cuda.synchronize(dev)
+    assert vef.device_status() == 0
+    ref = oracle_mod.forward(qn, kn, vn)
+    got = out.double().cpu().numpy()
+    diff = got - ref
+    mx = float(np.abs(diff).max())
+    rel = float(np.linalg.norm(diff) / np.linalg.norm(ref))
+    assert mx <= MAX_ABS and rel <= MAX_REL_L2, f"max abs {mx:.3e}, rel L2 {rel:.3e}"

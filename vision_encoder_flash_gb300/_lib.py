@@ -57,6 +57,16 @@ def load_library():
     lib.vattn_forward_host.restype = ctypes.c_int
     lib.vattn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.vattn_forward_noalloc.restype = ctypes.c_int
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.vattn_forward_mode.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ip]
+    lib.vattn_forward_mode.restype = ctypes.c_int
+    lib.vattn_forward_mode_for.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ip]
+    lib.vattn_forward_mode_for.restype = ctypes.c_int
+    lib.vattn_set_single_kernel.argtypes = [ctypes.c_int]
+    lib.vattn_set_single_kernel.restype = ctypes.c_int
+    lib.vattn_set_split_tiles.argtypes = [ctypes.c_int]
+    lib.vattn_set_split_tiles.restype = ctypes.c_int
     lib.vattn_selftest_wait_timeout.argtypes = [vp]
     lib.vattn_selftest_wait_timeout.restype = ctypes.c_int
     lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -179,6 +189,42 @@ def forward_noalloc_status(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patch
     """Like forward_noalloc_raw but returns the status code instead of raising."""
     return int(load_library().vattn_forward_noalloc(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
                                                     n_patches, head_dim, stream))
+
+
+# vattn_mode values
+MODE_NONE, MODE_DIRECT, MODE_SINGLE_KERNEL, MODE_TWO_KERNELS = 0, 1, 2, 3
+
+
+def forward_mode(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_dim) -> int:
+    """The kernel mode (MODE_*) vattn_forward takes for these device arguments
+    on the current device (vattn_forward_mode); raises on argument errors."""
+    mode = ctypes.c_int(-1)
+    _check(load_library().vattn_forward_mode(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads,
+                                             n_patches, head_dim, ctypes.byref(mode)))
+    return int(mode.value)
+
+
+def forward_mode_for(batch, n_heads, n_patches, head_dim, aligned, cooperative_launch,
+                     blocks_per_sm) -> int:
+    """The mode rule with the device facts passed in (vattn_forward_mode_for,
+    no CUDA call); raises on argument errors."""
+    mode = ctypes.c_int(-1)
+    _check(load_library().vattn_forward_mode_for(batch, n_heads, n_patches, head_dim, int(aligned),
+                                                 int(cooperative_launch), int(blocks_per_sm),
+                                                 ctypes.byref(mode)))
+    return int(mode.value)
+
+
+def set_single_kernel(allow: bool) -> bool:
+    """Allow or forbid the single cooperative kernel process-wide; returns the
+    previous setting."""
+    return bool(load_library().vattn_set_single_kernel(1 if allow else 0))
+
+
+def set_split_tiles(allow: bool) -> bool:
+    """Allow or forbid cut work tiles (balanced last round) process-wide;
+    returns the previous setting."""
+    return bool(load_library().vattn_set_split_tiles(1 if allow else 0))
 
 
 def selftest_wait_timeout(stream: int = 0) -> None:

@@ -91,6 +91,7 @@ enum WaitSite : uint32_t {
   kSiteMmaSFree = 14,
   kSiteConvert = 16,
   kSiteKvReady = 17,
+  kSitePartial = 18,
 };
 constexpr uint32_t kStatusTimeout = 0x100u;
 
@@ -113,7 +114,73 @@ struct Params {
   uint16_t* k16;
   uint16_t* v16;
   uint32_t* kv_ready;
+  // Work schedule (see Sched): `rounds` rounds of whole tiles, one more
+  // whole tile for the first `extra` blocks, then the remaining tiles' key
+  // tiles (tail_units of them) cut into one contiguous range per block.  A
+  // tile cut between blocks b and b + 1 is finished by whichever of its two
+  // parts ends second: the first one leaves its partial (O, m, l) in
+  // part[slot b] and raises its flag in part_sync, the second merges.
+  int rounds;
+  int extra;
+  long long tail_units;
+  float* part;          // [n_blocks - 1][NQ][128 rows x (d_pad + 2)] f32, or null
+  uint32_t* part_sync;  // [n_blocks - 1][NQ][4 warps][2]: arrival count, ready flag; zero at launch
 };
+
+// A block's share of the work, in order: whole tiles blockIdx.x + r *
+// gridDim.x for r < rounds, whole tile blockIdx.x + rounds * gridDim.x if
+// blockIdx.x < extra, then the key-tile units [u0, u1) of its range of the
+// tail (tiles (rounds + (extra > 0)) * gridDim.x onwards, unit u = key tile
+// u % T of tail tile u / T).  A schedule has either whole extra tiles or a
+// tail.  Every range of the tail holds at least T units (the host chooses
+// `rounds` so), so a tile is cut at most once, between two neighbouring
+// blocks.
+struct Piece {
+  int tile;  // bh * n_qblocks + query block
+  int j0;    // key tiles [j0, j1)
+  int j1;
+  int slot;  // partial slot of a cut tile (-1: a whole tile)
+};
+
+// The block's schedule, computed once by thread 0 into shared memory (so
+// that no role keeps it in registers) and read back per piece.
+struct Sched {
+  int whole;      // whole tiles of this block: rounds (+ 1 if blockIdx.x < extra)
+  int tail_base;  // first tile of the tail
+  int x0, jf;     // the first tail piece: tail tile x0 from key tile jf
+  int x1, jl;     // the last tail piece: tail tile x1 up to key tile jl (exclusive)
+  int n;          // pieces of this block
+
+  __device__ __forceinline__ static Sched make(const Params& p, int T) {
+    Sched s;
+    const int G = static_cast<int>(gridDim.x);
+    const int b = static_cast<int>(blockIdx.x);
+    s.whole = p.rounds + (b < p.extra ? 1 : 0);
+    s.tail_base = p.rounds * G;
+    const long long u0 = static_cast<long long>(b) * p.tail_units / G;
+    const long long u1 = static_cast<long long>(b + 1) * p.tail_units / G;
+    s.x0 = static_cast<int>(u0 / T);
+    s.jf = static_cast<int>(u0 - static_cast<long long>(s.x0) * T);
+    s.x1 = u1 > u0 ? static_cast<int>((u1 - 1) / T) : s.x0 - 1;
+    s.jl = u1 > u0 ? static_cast<int>(u1 - static_cast<long long>(s.x1) * T) : 0;
+    s.n = s.whole + (s.x1 - s.x0 + 1);
+    return s;
+  }
+};
+
+// Piece i of the block whose Sched sits in shared memory at `sp`.
+__device__ __forceinline__ Piece piece_at(const volatile Sched* sp, int i, int T) {
+  const int b = static_cast<int>(blockIdx.x);
+  if (i < sp->whole) return Piece{b + i * static_cast<int>(gridDim.x), 0, T, -1};
+  const int x0 = sp->x0;
+  const int x = x0 + (i - sp->whole);
+  Piece pc;
+  pc.tile = sp->tail_base + x;
+  pc.j0 = x == x0 ? sp->jf : 0;
+  pc.j1 = x == sp->x1 ? sp->jl : T;
+  pc.slot = pc.j0 > 0 ? b - 1 : (pc.j1 < T ? b : -1);
+  return pc;
+}
 
 // Shared-memory plan for NQ query tiles and NKB 64-column blocks of d_pad.
 // f16 tiles: NKB blocks of [128 rows x 128 bytes], 128-byte swizzle.
@@ -214,7 +281,8 @@ enum Bar : int {
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
 constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
 constexpr int kConvOkOff = kAbortOff + 4;    // u32: kInStageKV slot wait result, for the warpgroup
-static_assert(kConvOkOff + 4 <= 512, "barrier block overflow");
+constexpr int kSchedOff = kConvOkOff + 4;    // Sched of the block
+static_assert(kSchedOff + sizeof(Sched) <= 512, "barrier block overflow");
 
 struct Waiter {
   volatile uint32_t* abort_flag;
@@ -330,13 +398,12 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int N = p.n_patches;
   const int T = p.n_ktiles;
-  // Tiles of this block: blockIdx.x, blockIdx.x + gridDim.x, ... (the grid
-  // has at most n_tiles blocks, so every block has at least one).
-  const int n_mine = (p.n_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                     static_cast<int>(gridDim.x);
-  auto tile_of = [&](int i) -> int { return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x); };
-  auto tile_bh = [&](int i) -> int { return tile_of(i) / p.n_qblocks; };
-  auto tile_row0 = [&](int i) -> int { return (tile_of(i) % p.n_qblocks) * (kBM * NQ); };
+  // The pieces of work of this block (Sched, in shared memory once the
+  // block's first barrier has passed); every block has at least one.
+  const volatile Sched* sched_s = reinterpret_cast<const volatile Sched*>(base + P::kOffBar + kSchedOff);
+  auto sched = [&](int i) -> Piece { return piece_at(sched_s, i, T); };
+  auto tile_bh = [&](int i) -> int { return sched(i).tile / p.n_qblocks; };
+  auto tile_row0 = [&](int i) -> int { return (sched(i).tile % p.n_qblocks) * (kBM * NQ); };
 
   // Key tiles are numbered across the tiles of the block (g = i * T + j), so
   // every ring of barriers keeps its phase from one tile to the next.
@@ -374,6 +441,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
     }
     ptx::mbar_init(bar(kBarMmaDone), 2);
     *abort_flag = 0;
+    *reinterpret_cast<Sched*>(base + P::kOffBar + kSchedOff) = Sched::make(p, T);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -384,6 +452,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + P::kOffBar + kTmemSlotOff);
+  const int n_mine = sched_s->n;
   const uint32_t tile_bytes = static_cast<uint32_t>(P::kTileF16);
 
   const bool softmax_wg = warp >= 4 && warp < 4 + 4 * NQ;
@@ -517,17 +586,18 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
       return true;
     };
     bool ok = true;
+    int g = 0;  // key tiles of this block so far
     for (int i = 0; ok && i < n_mine; ++i) {
-      for (int j = 0; ok && j < T; ++j) {
-        const int64_t g = static_cast<int64_t>(i) * T + j;
+      const int j0 = sched(i).j0, j1 = sched(i).j1;
+      for (int j = j0; ok && j < j1; ++j, ++g) {
         const int st = kv_stage(g);
         const uint32_t free_par = kv_phase(g) ^ 1u;
         if (!(ok = w.wait_warp(bar(kBarKEmpty + st), free_par, kSiteConvert))) break;
         if (!(ok = convert(base_s + P::kOffK + st * P::kStageStride, kBarKFull + st))) break;
         if (!(ok = w.wait_warp(bar(kBarVEmpty + st), free_par, kSiteConvert))) break;
         if (!(ok = convert(base_s + P::kOffV + st * P::kStageStride, kBarVFull + st))) break;
-        if (j == 0) {
-          // the Q tiles of tile i, once the S products of tile i - 1 are done
+        if (j == j0) {
+          // the Q tiles of piece i, once the S products of piece i - 1 are done
           if (i > 0 && !(ok = w.wait_warp(bar(kBarQEmpty), static_cast<uint32_t>(i - 1) & 1u,
                                           kSiteConvert)))
             break;
@@ -559,11 +629,13 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
         };
         bool ok = true;
         for (int i = 0; ok && i < n_mine; ++i) {
-          const int bh = tile_bh(i);
-          for (int j = 0; ok && j < T; ++j) {
+          const Piece pc = sched(i);
+          const int bh = pc.tile / p.n_qblocks;
+          const int row0 = (pc.tile % p.n_qblocks) * (kBM * NQ);
+          for (int j = pc.j0; ok && j < pc.j1; ++j) {
             ok = load(&tm_k, j * kBN, bh) && load(&tm_v, j * kBN, bh);
-            for (int t = 0; ok && j == 0 && t < NQ; ++t)
-              ok = load(&tm_q, tile_row0(i) + t * kBM, bh);
+            for (int t = 0; ok && j == pc.j0 && t < NQ; ++t)
+              ok = load(&tm_q, row0 + t * kBM, bh);
           }
         }
         // every issued copy must have landed before the block exits
@@ -585,10 +657,11 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
         }
         int64_t k_issued = 0, v_issued = 0;
         bool ok = true;
+        int g = 0;  // key tiles of this block so far
         for (int i = 0; ok && i < n_mine; ++i) {
-          const int bh = tile_bh(i);
-          for (int j = 0; j < T; ++j) {
-            const int64_t g = static_cast<int64_t>(i) * T + j;
+          const Piece pc = sched(i);
+          const int bh = pc.tile / p.n_qblocks;
+          for (int j = pc.j0; j < pc.j1; ++j, ++g) {
             const int st = kv_stage(g);
             const uint32_t free_par = kv_phase(g) ^ 1u;
             if constexpr (P::kStageKV) {
@@ -729,6 +802,20 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
           const uint32_t qa = base_s + P::kOffQ + t * P::kStageStride;
           const uint32_t kb = base_s + P::kOffK + kv_stage(g) * P::kStageStride;
           const uint32_t d = tmem + static_cast<uint32_t>(sbuf(t, g)) * 128u;
+          if constexpr (!kAcc && NKB == 1) {
+            if (ksteps == 4) {
+              // head_dim 49..64: the descriptors as 32-bit halves, one add per
+              // product (fewer instructions between the blocking issues)
+              constexpr uint32_t hi = ptx::smem_desc_hi(1024, ptx::kSwizzle128B);
+              const uint32_t qlo = ptx::smem_desc_lo(qa, 16), klo = ptx::smem_desc_lo(kb, 16);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                ptx::mma_ss(d, ptx::smem_desc_join(qlo + 2u * ks, hi),
+                            ptx::smem_desc_join(klo + 2u * ks, hi), idesc_s, ks > 0 ? 1u : 0u);
+              ptx::mma_commit(bar(kBarSFull + sbuf(t, g)));
+              return;
+            }
+          }
           for (int ks = 0; ks < ksteps; ++ks) {
             const uint32_t off = static_cast<uint32_t>((ks >> 2) * kBoxBytes + (ks & 3) * 32);
             ptx::mma_ss(d, ptx::smem_desc(qa + off, 16, 1024, ptx::kSwizzle128B),
@@ -745,20 +832,21 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
           ptx::mma_commit(bar(kBarSFull + sbuf(t, g)));
         };
         bool ok = true;
+        int g = 0;  // key tiles of this block so far
         for (int i = 0; ok && i < n_mine; ++i) {
           if (!(ok = w.wait(bar(kBarQFull), static_cast<uint32_t>(i) & 1u, kSiteMmaQ))) break;
-          for (int j = 0; j < T; ++j) {
-            const int64_t g = static_cast<int64_t>(i) * T + j;
+          const Piece pc = sched(i);
+          for (int j = pc.j0; j < pc.j1; ++j, ++g) {
             // S of key tile g needs K_g and the softmax to have copied the
             // previous contents of its buffer(s) to registers
             if (!(ok = w.wait(bar(kBarKFull + kv_stage(g)), kv_phase(g), kSiteMmaK))) break;
-            const int64_t prev = NQ == 2 ? g - 1 : g - 2;  // last key tile that used the buffer(s)
+            const int prev = NQ == 2 ? g - 1 : g - 2;  // last key tile that used the buffer(s)
             if (prev >= 0 &&
                 !(ok = w.wait(bar(kBarSFree + sfree_bar(prev)), sphase(prev), kSiteMmaSFree)))
               break;
             ptx::tc_fence_after();
             for (int t = 0; t < NQ; ++t) {
-              if (P::kF32Q && j == 0 && t == 1) {  // Q tile 1 is rounded after tile 0
+              if (P::kF32Q && j == pc.j0 && t == 1) {  // Q tile 1 is rounded after tile 0
                 if (!(ok = w.wait(bar(kBarQFull1), static_cast<uint32_t>(i) & 1u, kSiteMmaQ))) break;
                 ptx::tc_fence_after();
               }
@@ -795,9 +883,10 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
           ptx::mma_commit(bar(kBarODone + t));
         };
         bool ok = true;
+        int g = 0;  // key tiles of this block so far
         for (int i = 0; ok && i < n_mine; ++i) {
-          for (int j = 0; j < T; ++j) {
-            const int64_t g = static_cast<int64_t>(i) * T + j;
+          const Piece pc = sched(i);
+          for (int j = pc.j0; j < pc.j1; ++j, ++g) {
             if (!(ok = w.wait(bar(kBarVFull + kv_stage(g)), kv_phase(g), kSiteMmaV))) break;
             // P of key tile g written (for the first key tile of a tile this
             // also tells that the softmax has read the previous tile's O)
@@ -806,13 +895,13 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
               for (int t = 0; ok && t < NQ; ++t) {
                 if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
                 ptx::tc_fence_after();
-                issue_pv(t, g, j == 0);
+                issue_pv(t, g, j == pc.j0);
               }
               if (!ok) break;
             } else {
               if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
               ptx::tc_fence_after();
-              for (int t = 0; t < NQ; ++t) issue_pv(t, g, j == 0);
+              for (int t = 0; t < NQ; ++t) issue_pv(t, g, j == pc.j0);
             }
             ptx::mma_commit(bar(kBarVEmpty + kv_stage(g)));
           }
@@ -829,11 +918,12 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
     const uint32_t p_addr = tmem + lane_addr + P::kColP + static_cast<uint32_t>(t) * P::kColPStride;
     const uint32_t o_addr = tmem + lane_addr + P::kColO + static_cast<uint32_t>(t) * P::kColOStride;
     bool ok = true;
+    int g = 0;  // key tiles of this block so far
     for (int i = 0; ok && i < n_mine; ++i) {
+      const int j0 = sched(i).j0, j1 = sched(i).j1;
       float m_ref = -INFINITY;  // running max in log2 units (may lag the true max by < 8)
       float l = 0.0f;           // running sum of exp2(s*log2e - m_ref)
-      int64_t g = static_cast<int64_t>(i) * T;
-      for (int j = 0; j < T; ++j, ++g) {
+      for (int j = j0; j < j1; ++j, ++g) {
         const int buf = sbuf(t, g);
         if (!(ok = w.wait_warp(bar(kBarSFull + buf), sphase(g), kSiteSoftS))) break;
         ptx::tc_fence_after();
@@ -912,15 +1002,15 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
               break;
             ptx::tc_fence_after();
           }
-        } else if (j > 0) {
+        } else if (j > j0) {
           // P V of the previous key tile has finished: P buffer free, O final.
-          // (For j == 0 the previous tile's epilogue already waited for it.)
+          // (For a piece's first key tile the previous epilogue waited for it.)
           if (!(ok = w.wait_warp(bar(kBarODone + t), static_cast<uint32_t>((g - 1) & 1),
                                  kSiteSoftO)))
             break;
           ptx::tc_fence_after();
         }
-        if (j > 0) {
+        if (j > j0) {
           if (__any_sync(0xffffffffu, need)) {
             for (int c = 0; c < (p.d_pad >> 4); ++c) {
               uint32_t y[16];
@@ -952,6 +1042,67 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
                              kSiteEpilogue)))
         break;
       ptx::tc_fence_after();
+      const Piece pc = sched(i);
+      if (pc.slot >= 0) {
+        // A tile cut between two neighbouring blocks (keys [0, c) in one,
+        // [c, T) in the other).  The part that ends first leaves its O
+        // (unnormalised), m and l in the slot and raises the slot's flag; the
+        // part that ends second waits for the flag (the other part is then
+        // already writing it), adds the partial into its own O by the
+        // log-sum-exp rule -- the shader's rescale of (m, l, o) by the
+        // larger of the two maxima -- and stores the tile as usual.
+        // Each warp (its 32 rows) meets its counterpart on its own: arrival
+        // count and flag per (slot, query tile, warp), no block-wide barrier.
+        const size_t slot_floats = static_cast<size_t>(kBM) * static_cast<size_t>(p.d_pad + 2);
+        float* part = p.part + (static_cast<size_t>(pc.slot) * NQ + t) * slot_floats;
+        float4* part4 = reinterpret_cast<float4*>(part);  // column group c4 of row r at c4 * 128 + r
+        uint32_t* sync = p.part_sync + ((static_cast<size_t>(pc.slot) * NQ + t) * 4 + quarter) * 2;
+        uint32_t order = 0;
+        if (lane == 0) order = atomicAdd(sync, 1u);
+        const bool second = __shfl_sync(0xffffffffu, order, 0) != 0u;
+        const int r = quarter * 32 + lane;
+        if (!second) {
+          for (int c = 0; c < (p.d_pad >> 4); ++c) {
+            uint32_t y[16];
+            ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
+            ptx::tmem_wait_ld_dep16(y);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              part4[(c * 4 + k) * kBM + r] =
+                  make_float4(__uint_as_float(y[4 * k]), __uint_as_float(y[4 * k + 1]),
+                              __uint_as_float(y[4 * k + 2]), __uint_as_float(y[4 * k + 3]));
+          }
+          part[kBM * p.d_pad + r] = m_ref;
+          part[kBM * (p.d_pad + 1) + r] = l;
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) ptx::st_release_gpu(sync + 1, 1u);
+          ptx::tc_fence_before();
+          continue;
+        }
+        if (!(ok = __all_sync(0xffffffffu, w.wait_flag(sync + 1, kSitePartial)))) break;
+        const float mp = part[kBM * p.d_pad + r];
+        const float lp = part[kBM * (p.d_pad + 1) + r];
+        const float mx = fmaxf(m_ref, mp);
+        const float ca = ptx::ex2_approx(m_ref - mx);
+        const float cb = ptx::ex2_approx(mp - mx);
+        l = ca * l + cb * lp;
+        for (int c = 0; c < (p.d_pad >> 4); ++c) {
+          uint32_t y[16];
+          ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
+          ptx::tmem_wait_ld_dep16(y);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float4 z = part4[(c * 4 + k) * kBM + r];
+            y[4 * k + 0] = __float_as_uint(fmaf(__uint_as_float(y[4 * k + 0]), ca, z.x * cb));
+            y[4 * k + 1] = __float_as_uint(fmaf(__uint_as_float(y[4 * k + 1]), ca, z.y * cb));
+            y[4 * k + 2] = __float_as_uint(fmaf(__uint_as_float(y[4 * k + 2]), ca, z.z * cb));
+            y[4 * k + 3] = __float_as_uint(fmaf(__uint_as_float(y[4 * k + 3]), ca, z.w * cb));
+          }
+          ptx::tmem_st_32x32b_x16(o_addr + c * 16, y);
+        }
+        ptx::tmem_wait_st();
+      }
       const float inv_l = 1.0f / l;
       if (P::kEpiBytes > 0 && p.tma_out) {
         // 16 columns at a time: TMEM -> registers -> swizzled shared buffer
@@ -960,7 +1111,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
         // the background while the warp moves on to the next tile
         const uint32_t epi =
             base_s + P::kOffEpi + static_cast<uint32_t>(warp - 4) * 4096u;
-        const int row_base = tile_row0(i) + t * kBM + quarter * 32;
+        const int pc_bh = pc.tile / p.n_qblocks;
+        const int row_base = (pc.tile % p.n_qblocks) * (kBM * NQ) + t * kBM + quarter * 32;
         for (int c = 0; c < (p.d_pad >> 4); ++c) {
           uint32_t y[16];
           ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
@@ -997,17 +1149,18 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tm_o, buf, c * 16, row_base, tile_bh(i));
+            ptx::tma_store_3d(&tm_o, buf, c * 16, row_base, pc_bh);
             ptx::bulk_commit_group();
           }
         }
         ptx::tc_fence_before();
         continue;
       }
-      const int row = tile_row0(i) + t * kBM + quarter * 32 + lane;
+      const int row = (pc.tile % p.n_qblocks) * (kBM * NQ) + t * kBM + quarter * 32 + lane;
+      const int pc_bh = pc.tile / p.n_qblocks;
       const int D = p.head_dim;
       if constexpr (kOut16) {
-        uint16_t* orow16 = p.out16 + (static_cast<size_t>(tile_bh(i)) * N + row) * D;
+        uint16_t* orow16 = p.out16 + (static_cast<size_t>(pc_bh) * N + row) * D;
         for (int c = 0; c < (p.d_pad >> 4); ++c) {
           uint32_t y[16];
           ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);
@@ -1026,7 +1179,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
         ptx::tc_fence_before();
         continue;
       }
-      float* orow = p.out + (static_cast<size_t>(tile_bh(i)) * N + row) * D;
+      float* orow = p.out + (static_cast<size_t>(pc_bh) * N + row) * D;
       for (int c = 0; c < (p.d_pad >> 4); ++c) {
         uint32_t y[16];
         ptx::tmem_ld_32x32b_x16(o_addr + c * 16, y);

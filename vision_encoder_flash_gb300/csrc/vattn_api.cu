@@ -183,8 +183,48 @@ vattn_status sm_count(int device, int* out) {
   return VATTN_OK;
 }
 
+// Work schedule of the persistent attention kernel over n_tiles tiles of T
+// key tiles on `grid` blocks (the kernel's Sched).  Whole tiles in rounds;
+// when the rounds leave a last, partial round (n_tiles % grid != 0) and
+// cutting is allowed, the last one or two rounds' tiles are instead cut by
+// key ranges into one equal share per block -- provided that shortens the
+// busiest block by at least two key tiles, which pays for the merge of the
+// cut tiles.  Each share holds at least T key tiles (the tail has at least
+// `grid` tiles), so a tile is cut at most once.
+struct Schedule {
+  int rounds = 0;
+  int extra = 0;
+  long long tail_units = 0;
+  bool cut = false;
+};
+
+// Process-wide switch of vattn_set_split_tiles (off by default).
+std::atomic<int> g_cut_allowed{0};
+
+Schedule make_schedule(long long n_tiles, int T, int grid, bool allow_cut) {
+  Schedule s;
+  s.rounds = static_cast<int>(n_tiles / grid);
+  s.extra = static_cast<int>(n_tiles % grid);
+  if (!allow_cut || s.extra == 0 || grid < 2) return s;
+  const int r = n_tiles >= 2LL * grid ? s.rounds - 1 : 0;
+  const long long tail = (n_tiles - static_cast<long long>(r) * grid) * T;
+  const long long busiest_cut = static_cast<long long>(r) * T + (tail + grid - 1) / grid;
+  const long long busiest_whole = static_cast<long long>(s.rounds + 1) * T;
+  if (busiest_cut + 2 > busiest_whole) return s;
+  s.rounds = r;
+  s.extra = 0;
+  s.tail_units = tail;
+  s.cut = true;
+  return s;
+}
+
+// f32 words of one partial slot (a cut tile's O, m, l for its nq query tiles)
+size_t part_slot_floats(int nq, int d_pad) {
+  return static_cast<size_t>(nq) * vattn::kBM * static_cast<size_t>(d_pad + 2);
+}
+
 // The attention kernel is persistent: one block per multiprocessor (at most
-// one per tile), each looping over the tiles blockIdx.x + k * gridDim.x.
+// one per tile), each looping over its share of the work (make_schedule).
 // tql, tkl, tvl: the lo halves of q, k, v (accurate mode only; otherwise
 // unused and any valid map may be passed).
 template <int NQ, int NKB, bool kOut16, bool kAcc, int kIn = vattn::kInF16>
@@ -192,7 +232,7 @@ vattn_status launch_attention_maps(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const CUtensorMap& tql,
                                    const CUtensorMap& tkl, const CUtensorMap& tvl,
                                    vattn::Params p, unsigned n_tiles, cudaStream_t stream,
-                                   int device) {
+                                   int device, bool* coop_refused = nullptr) {
   using P = vattn::Plan<NQ, NKB, kAcc, kIn>;
   auto kernel = vattn::vattn_fwd_kernel<NQ, NKB, kOut16, kAcc, kIn>;
   static std::atomic<uint8_t> configured[kMaxDevices];
@@ -206,6 +246,11 @@ vattn_status launch_attention_maps(const CUtensorMap& tq, const CUtensorMap& tk,
   const vattn_status st = sm_count(device, &sms);
   if (st != VATTN_OK) return st;
   const unsigned grid = n_tiles < static_cast<unsigned>(sms) ? n_tiles : static_cast<unsigned>(sms);
+  if (p.rounds == 0 && p.extra == 0 && p.tail_units == 0) {
+    // no schedule given: whole tiles, round robin over the blocks
+    p.rounds = static_cast<int>(n_tiles / grid);
+    p.extra = static_cast<int>(n_tiles % grid);
+  }
   // the output goes through TMA stores when the kernel variant stages it
   // (head_dim <= 64) and its rows are whole 16-byte units
   CUtensorMap to;
@@ -240,6 +285,12 @@ vattn_status launch_attention_maps(const CUtensorMap& tq, const CUtensorMap& tk,
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, tql, tkl, tvl, p);
   if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaErrorCooperativeLaunchTooLarge && coop_refused != nullptr) {
+    // not sticky: the caller takes another mode
+    (void)cudaGetLastError();
+    *coop_refused = true;
+    return cuda_fail(e, "cooperative attention kernel launch");
+  }
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   return VATTN_OK;
 }
@@ -268,35 +319,27 @@ int query_tiles(int n_patches, int d_pad) {
 // single kernel is 1.65x faster than staging + attention at 256 patches,
 // 1.23x at 1024, even at 2048 and 0.98x at 2304.  Narrower heads stage
 // cheaper (head_dim 32 at 1024 patches: 0.96x), so they keep the two passes.
-bool f32_direct(const float* q, const float* k, const float* v, int N, int D) {
+bool direct_shape(int N, int D) {
   const int d_pad = (D + 15) & ~15;
-  return d_pad <= 64 && D > 32 && D % 4 == 0 && N <= 2048 && query_tiles(N, d_pad) == 2 &&
-         ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+  return d_pad <= 64 && D > 32 && D % 4 == 0 && N <= 2048 && query_tiles(N, d_pad) == 2;
+}
+
+bool aligned16(const void* q, const void* k, const void* v) {
+  return ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
            reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
 }
 
-// The attention kernel on f32 inputs (f32_direct(...) holds): one launch.
-vattn_status launch_f32_direct(const float* q, const float* k, const float* v, float* out,
+// The attention kernel on f32 inputs (direct_shape and aligned16 hold): one launch;
+// p carries the tiling and the work schedule.
+vattn_status launch_f32_direct(const float* q, const float* k, const float* v, vattn::Params p,
                                int64_t bh, int N, int D, cudaStream_t stream, int device) {
-  const int64_t n_qblocks = (N + 2 * vattn::kBM - 1) / (2 * vattn::kBM);
-  const int64_t grid = bh * n_qblocks;
-  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
-  vattn::Params p{};
-  p.out = out;
-  p.n_patches = N;
-  p.head_dim = D;
-  p.d_pad = (D + 15) & ~15;
-  p.n_qblocks = static_cast<int>(n_qblocks);
-  p.n_tiles = static_cast<int>(grid);
-  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
-  p.vec_out = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
   CUtensorMap tq, tk, tv;
   vattn_status st;
   if ((st = make_tmap32(&tq, q, bh, N, D)) != VATTN_OK) return st;
   if ((st = make_tmap32(&tk, k, bh, N, D)) != VATTN_OK) return st;
   if ((st = make_tmap32(&tv, v, bh, N, D)) != VATTN_OK) return st;
   return launch_attention_maps<2, 1, false, false, vattn::kInF32>(
-      tq, tk, tv, tq, tk, tv, p, static_cast<unsigned>(grid), stream, device);
+      tq, tk, tv, tq, tk, tv, p, static_cast<unsigned>(p.n_tiles), stream, device);
 }
 
 // The kernel variant for nkb 64-column blocks of d_pad and nq query tiles.
@@ -495,66 +538,202 @@ vattn_status launch_conv1d4(const vattn::Conv1dArgs& a, int device, int sms, cud
                           sms, stream);
 }
 
-// The kernels of vattn_forward on device tensors of bh heads, with the f16
-// workspace ws (three regions of `region` bytes) supplied by the caller:
-// the direct f32 kernel where it applies, else the staging kernel and the
-// attention kernel.  With two query tiles of head_dim <= 64 the attention
-// kernel reads q in f32 and rounds it itself (q is read once per work tile,
-// so that costs it little) and the staging kernel rounds k and v alone.
-// single_kernel: the k and v staging may run inside the attention kernel
-// (a cooperative launch); vattn_forward_host passes false: with it, its
-// chunked calls measured 12 % slower end to end (1.55 against 1.37 ms at
-// 8 x 16 heads, 2304 patches), where the copies, not the kernels, set the
-// time.
-// Arguments are valid (checked by the entry points).
-vattn_status run_forward(const float* q, const float* k, const float* v, float* out, int64_t bh,
-                         int N, int D, void* ws, size_t region, cudaStream_t stream, int device,
-                         bool single_kernel = true) {
-  if (f32_direct(q, k, v, N, D)) return launch_f32_direct(q, k, v, out, bh, N, D, stream, device);
+// ---------------------------------------------------------------- mode choice
+// The single cooperative kernel (k and v staged inside it) needs every block
+// of its grid resident at once: the device must support cooperative launches
+// and hold one of its 512-thread, ~231 KB blocks per multiprocessor.  Both
+// facts are read once per device; vattn_set_single_kernel(0) forbids the mode
+// process-wide (the calls then take the two-kernel mode, bit-identical).
+struct SingleKernelFacts {
+  std::once_flag once;
+  int cooperative = 0;    // cudaDevAttrCooperativeLaunch
+  int blocks_per_sm = 0;  // resident blocks of the kernel per multiprocessor
+  cudaError_t err = cudaSuccess;
+};
+SingleKernelFacts g_single_facts[kMaxDevices];
+std::atomic<int> g_single_kernel_allowed{1};
+
+using SingleKernelPlan = vattn::Plan<2, 1, false, vattn::kInStageKV>;
+
+vattn_status single_kernel_facts(int device, int* cooperative, int* blocks_per_sm) {
+  if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
+  SingleKernelFacts& f = g_single_facts[device];
+  std::call_once(f.once, [&f, device] {
+    f.err = cudaDeviceGetAttribute(&f.cooperative, cudaDevAttrCooperativeLaunch, device);
+    if (f.err != cudaSuccess) return;
+    auto kernel = vattn::vattn_fwd_kernel<2, 1, false, false, vattn::kInStageKV>;
+    // the occupancy query counts dynamic shared memory only up to the
+    // kernel's opt-in limit, so raise it first (the launch does the same)
+    f.err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SingleKernelPlan::kSmemBytes);
+    if (f.err != cudaSuccess) return;
+    f.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.blocks_per_sm, kernel,
+                                                          SingleKernelPlan::kThreads,
+                                                          SingleKernelPlan::kSmemBytes);
+  });
+  if (f.err != cudaSuccess) return cuda_fail(f.err, "querying cooperative launch support");
+  *cooperative = f.cooperative;
+  *blocks_per_sm = f.blocks_per_sm;
+  return VATTN_OK;
+}
+
+// The kernels a vattn_forward call on a non-empty, valid problem runs, from
+// its sizes, whether q, k and v are all 16-byte aligned, and the device
+// facts above (single_allowed: the caller and the process-wide switch allow
+// the single cooperative kernel).
+vattn_mode forward_mode_rule(int N, int D, bool all_aligned16, bool single_allowed,
+                             int cooperative, int blocks_per_sm) {
   const int d_pad = (D + 15) & ~15;
+  if (all_aligned16 && direct_shape(N, D)) return VATTN_MODE_DIRECT;
   const int nkb = d_pad <= 64 ? 1 : 2;
-  const int nq = query_tiles(N, d_pad);
-  const int64_t n_qblocks = (N + vattn::kBM * nq - 1) / (vattn::kBM * nq);
-  const int64_t grid = bh * n_qblocks;
-  if (grid > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+  const bool q_f32 = nkb == 1 && query_tiles(N, d_pad) == 2 && D % 4 == 0;
+  if (single_allowed && all_aligned16 && q_f32 && cooperative != 0 && blocks_per_sm >= 1)
+    return VATTN_MODE_SINGLE_KERNEL;
+  return VATTN_MODE_TWO_KERNELS;
+}
+
+// The mode a call takes on `device` (sizes and pointers already checked).
+vattn_status forward_mode_on(int device, const float* q, const float* k, const float* v, int N,
+                             int D, bool single_kernel, vattn_mode* mode) {
+  int coop = 0, blocks = 0;
+  const bool allowed = single_kernel && g_single_kernel_allowed.load(std::memory_order_relaxed) != 0;
+  const bool al = aligned16(q, k, v);
+  // the facts are read only when the rule could take the single kernel
+  if (allowed && forward_mode_rule(N, D, al, true, 1, 1) == VATTN_MODE_SINGLE_KERNEL) {
+    const vattn_status st = single_kernel_facts(device, &coop, &blocks);
+    if (st != VATTN_OK) return st;
+  }
+  *mode = forward_mode_rule(N, D, al, allowed, coop, blocks);
+  return VATTN_OK;
+}
+
+// Everything a vattn_forward call decides before it launches: the mode, the
+// tiling, the work schedule and the workspace it needs, laid out as
+//   sync words | partial slots | f16 q | f16 k | f16 v
+// Sync words: two per (cut slot, query tile, softmax warp) -- arrival
+// count, ready flag --
+// then, in the single kernel's mode, one ready flag per (head, key tile);
+// one memset per call clears them.  Partial slots: one per block boundary
+// of a cut schedule.  The f16 copies: none in the direct mode.
+struct ForwardPlan {
+  vattn_mode mode = VATTN_MODE_TWO_KERNELS;
+  int N = 0, D = 0, d_pad = 0, nkb = 1, nq = 1, T = 0, grid = 0;
+  int64_t bh = 0, n_qblocks = 0, n_tiles = 0;
+  Schedule sched;
+  size_t cut_words = 0, flag_words = 0;
+  size_t sync_bytes = 0;  // 256-byte rounded
+  size_t part_bytes = 0;  // 256-byte rounded
+  size_t region = 0;      // one f16 copy, 256-byte rounded (0: none)
+  size_t total() const { return sync_bytes + part_bytes + 3 * region; }
+};
+
+size_t round256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+// single_kernel: the caller allows the single cooperative kernel (the
+// host-buffer entry point does not); max_sync_part_bytes: room for the sync
+// words and partial slots together (a cut schedule is taken only if they
+// fit; 0: never).  Arguments are valid and the problem is not empty
+// (checked by the entry points).
+vattn_status plan_forward(int device, const float* q, const float* k, const float* v, int64_t bh,
+                          int N, int D, bool single_kernel, size_t max_sync_part_bytes,
+                          ForwardPlan* out) {
+  ForwardPlan pl;
+  vattn_status st = forward_mode_on(device, q, k, v, N, D, single_kernel, &pl.mode);
+  if (st != VATTN_OK) return st;
+  pl.N = N;
+  pl.D = D;
+  pl.bh = bh;
+  pl.d_pad = (D + 15) & ~15;
+  pl.nkb = pl.d_pad <= 64 ? 1 : 2;
+  pl.nq = query_tiles(N, pl.d_pad);
+  pl.n_qblocks = (N + vattn::kBM * pl.nq - 1) / (vattn::kBM * pl.nq);
+  pl.n_tiles = bh * pl.n_qblocks;
+  if (pl.n_tiles > INT32_MAX) return fail(VATTN_ERR_UNSUPPORTED, "grid too large");
+  pl.T = (N + vattn::kBN - 1) / vattn::kBN;
+  int sms = 0;
+  if ((st = sm_count(device, &sms)) != VATTN_OK) return st;
+  pl.grid = static_cast<int>(pl.n_tiles < sms ? pl.n_tiles : sms);
+  if (pl.mode == VATTN_MODE_SINGLE_KERNEL) pl.flag_words = static_cast<size_t>(bh) * pl.T;
+  const size_t slot_bytes = part_slot_floats(pl.nq, pl.d_pad) * sizeof(float);
+  const size_t cut_words = static_cast<size_t>(pl.grid - 1) * pl.nq * 4 * 2;
+  const size_t cut_need = round256((cut_words + pl.flag_words) * sizeof(uint32_t)) +
+                          round256(static_cast<size_t>(pl.grid - 1) * slot_bytes);
+  pl.sched = make_schedule(pl.n_tiles, pl.T, pl.grid,
+                           cut_need <= max_sync_part_bytes &&
+                               g_cut_allowed.load(std::memory_order_relaxed) != 0);
+  if (pl.sched.cut) {
+    pl.cut_words = cut_words;
+    pl.part_bytes = round256(static_cast<size_t>(pl.grid - 1) * slot_bytes);
+  }
+  pl.sync_bytes = round256((pl.cut_words + pl.flag_words) * sizeof(uint32_t));
+  if (pl.mode != VATTN_MODE_DIRECT)
+    pl.region = round256(static_cast<size_t>(bh) * N * pl.d_pad * 2);
+  *out = pl;
+  return VATTN_OK;
+}
+
+// The kernels of a planned vattn_forward call: sync (plan.sync_bytes) and
+// part (plan.part_bytes) and staging (3 regions of plan.region) are the
+// caller's workspace.  One memset clears the sync words; then the direct
+// f32 kernel, or the single cooperative kernel, or the staging kernel and
+// the attention kernel.  With two query tiles of head_dim <= 64 the
+// attention kernel reads q in f32 and rounds it itself (q is read once per
+// work tile, so that costs it little) and the staging kernel rounds k and v
+// alone.  A cooperative grid that the device refuses at launch (for example
+// under an MPS limit on multiprocessors) gets the two kernels instead.
+vattn_status run_forward(const ForwardPlan& pl, const float* q, const float* k, const float* v,
+                         float* out, uint32_t* sync, float* part, void* staging,
+                         cudaStream_t stream, int device) {
+  const int N = pl.N, D = pl.D, d_pad = pl.d_pad, nkb = pl.nkb, nq = pl.nq;
+  const int64_t bh = pl.bh;
+  if (pl.sync_bytes > 0) {
+    const cudaError_t e = cudaMemsetAsync(sync, 0, pl.sync_bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace flags");
+  }
   vattn::Params p{};
   p.out = out;
   p.n_patches = N;
   p.head_dim = D;
   p.d_pad = d_pad;
-  p.n_qblocks = static_cast<int>(n_qblocks);
-  p.n_tiles = static_cast<int>(grid);
-  p.n_ktiles = (N + vattn::kBN - 1) / vattn::kBN;
+  p.n_qblocks = static_cast<int>(pl.n_qblocks);
+  p.n_tiles = static_cast<int>(pl.n_tiles);
+  p.n_ktiles = pl.T;
   p.vec_out = (D % 4 == 0) && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  p.rounds = pl.sched.rounds;
+  p.extra = pl.sched.extra;
+  p.tail_units = pl.sched.tail_units;
+  p.part = pl.sched.cut ? part : nullptr;
+  p.part_sync = pl.sched.cut ? sync : nullptr;
+  if (pl.mode == VATTN_MODE_DIRECT) return launch_f32_direct(q, k, v, p, bh, N, D, stream, device);
+  const int64_t grid = pl.n_tiles;
   const bool q_f32 = nkb == 1 && nq == 2 && D % 4 == 0 && (reinterpret_cast<uintptr_t>(q) & 15u) == 0;
-  const bool kv_in_kernel = single_kernel && q_f32 &&
-                            ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
-  __half* q16 = static_cast<__half*>(ws);
-  __half* k16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + region);
-  __half* v16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + 2 * region);
+  __half* q16 = static_cast<__half*>(staging);
+  __half* k16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(staging) + pl.region);
+  __half* v16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(staging) + 2 * pl.region);
   CUtensorMap tq, tk, tv;
   vattn_status st;
   if ((st = q_f32 ? make_tmap32(&tq, q, bh, N, D) : make_tmap16(&tq, q16, bh, N, d_pad)) != VATTN_OK)
     return st;
   if ((st = make_tmap16(&tk, k16, bh, N, d_pad)) != VATTN_OK) return st;
   if ((st = make_tmap16(&tv, v16, bh, N, d_pad)) != VATTN_OK) return st;
-  if (kv_in_kernel) {
+  if (pl.mode == VATTN_MODE_SINGLE_KERNEL) {
     // one kernel: it writes the f16 copies of k and v itself, each key tile
-    // once, and the blocks that read a tile wait for its ready flag (the
-    // flags sit in the region of the q copy, which this path does not use)
-    uint32_t* flags = reinterpret_cast<uint32_t*>(q16);
-    const size_t flag_bytes = static_cast<size_t>(bh) * p.n_ktiles * sizeof(uint32_t);
-    const cudaError_t e = cudaMemsetAsync(flags, 0, flag_bytes, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the key-tile flags");
+    // once, and the blocks that read a tile wait for its ready flag (after
+    // the cut-tile words in the sync block)
     p.k16 = reinterpret_cast<uint16_t*>(k16);
     p.v16 = reinterpret_cast<uint16_t*>(v16);
-    p.kv_ready = flags;
+    p.kv_ready = sync + pl.cut_words;
     CUtensorMap tk32, tv32;  // the f32 tiles the kernel stages from
     vattn_status sm;
     if ((sm = make_tmap32(&tk32, k, bh, N, D)) != VATTN_OK) return sm;
     if ((sm = make_tmap32(&tv32, v, bh, N, D)) != VATTN_OK) return sm;
-    return launch_attention_maps<2, 1, false, false, vattn::kInStageKV>(
-        tq, tk, tv, tq, tk32, tv32, p, static_cast<unsigned>(grid), stream, device);
+    bool refused = false;
+    sm = launch_attention_maps<2, 1, false, false, vattn::kInStageKV>(
+        tq, tk, tv, tq, tk32, tv32, p, static_cast<unsigned>(grid), stream, device, &refused);
+    if (!refused) return sm;
+    g_last_error[0] = '\0';
+    p.k16 = p.v16 = nullptr;
+    p.kv_ready = nullptr;
   }
   const int64_t rows = bh * N;
   const uintptr_t src_or = (q_f32 ? 0u : reinterpret_cast<uintptr_t>(q)) |
@@ -654,18 +833,22 @@ vattn_status vattn_forward(const float* q, const float* k, const float* v, float
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  if (f32_direct(q, k, v, N, D)) return launch_f32_direct(q, k, v, out, bh, N, D, stream, device);
-
-  // f16 copies ([B*H, N, d_pad] each), stream-ordered workspace
-  const size_t region =
-      (static_cast<size_t>(bh) * N * d_pad * 2 + 255) & ~static_cast<size_t>(255);
-  cudaMemPool_t pool = nullptr;
-  vattn_status st = pool_for(device, &pool);
+  (void)d_pad;
+  ForwardPlan pl;
+  vattn_status st = plan_forward(device, q, k, v, bh, N, D, true, SIZE_MAX, &pl);
   if (st != VATTN_OK) return st;
+  if (pl.total() == 0) return run_forward(pl, q, k, v, out, nullptr, nullptr, nullptr, stream, device);
+
+  // sync words, partial slots and f16 copies: stream-ordered workspace
+  cudaMemPool_t pool = nullptr;
+  if ((st = pool_for(device, &pool)) != VATTN_OK) return st;
   void* ws = nullptr;
-  e = cudaMallocFromPoolAsync(&ws, 3 * region, pool, stream);
+  e = cudaMallocFromPoolAsync(&ws, pl.total(), pool, stream);
   if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
-  st = run_forward(q, k, v, out, bh, N, D, ws, region, stream, device);
+  uint8_t* const wb = static_cast<uint8_t*>(ws);
+  st = run_forward(pl, q, k, v, out, reinterpret_cast<uint32_t*>(wb),
+                   reinterpret_cast<float*>(wb + pl.sync_bytes), wb + pl.sync_bytes + pl.part_bytes,
+                   stream, device);
   // back to the pool once the launches above have run (stream order)
   e = cudaFreeAsync(ws, stream);
   if (st == VATTN_OK && e != cudaSuccess) st = cuda_fail(e, "workspace release");
@@ -1120,8 +1303,13 @@ vattn_status vattn_forward_host(const float* q, const float* k, const float* v, 
       // kernels; the output slot is free once the copy out of chunk c - 2 ran
       if (!ck(cudaStreamWaitEvent(s_comp, ev_in[c], 0), "cudaStreamWaitEvent")) break;
       if (c >= 2 && !ck(cudaStreamWaitEvent(s_comp, ev_out[c - 2], 0), "cudaStreamWaitEvent")) break;
-      st = run_forward(in_ptr(c, 0), in_ptr(c, 1), in_ptr(c, 2), out_ptr(c), hn, N, D, ws16,
-                       static_cast<size_t>(region), s_comp, device, false);
+      // the direct kernel, or the staging and attention kernels (no single
+      // cooperative kernel, no cut tiles: no sync words to clear)
+      ForwardPlan pl;
+      st = plan_forward(device, in_ptr(c, 0), in_ptr(c, 1), in_ptr(c, 2), hn, N, D, false, 0, &pl);
+      if (st == VATTN_OK)
+        st = run_forward(pl, in_ptr(c, 0), in_ptr(c, 1), in_ptr(c, 2), out_ptr(c), nullptr, nullptr,
+                         ws16, s_comp, device);
       if (st != VATTN_OK || !ck(cudaEventRecord(ev_comp[c], s_comp), "cudaEventRecord")) break;
       // copy out
       if (!ck(cudaStreamWaitEvent(s_out, ev_comp[c], 0), "cudaStreamWaitEvent") ||
@@ -1192,6 +1380,53 @@ const char* vattn_status_string(vattn_status status) {
   return "VATTN_ERR_UNKNOWN";
 }
 
+vattn_status vattn_forward_mode_for(int64_t batch, int64_t n_heads, int64_t n_patches,
+                                    int64_t head_dim, int aligned, int cooperative_launch,
+                                    int blocks_per_sm, int* mode) {
+  g_last_error[0] = '\0';
+  if (!mode) return fail(VATTN_ERR_INVALID_ARG, "null mode pointer");
+  *mode = VATTN_MODE_NONE;
+  const vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  if (batch * n_heads == 0 || n_patches == 0) return VATTN_OK;
+  if (n_patches > INT32_MAX || batch * n_heads > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  const bool allowed = g_single_kernel_allowed.load(std::memory_order_relaxed) != 0;
+  *mode = forward_mode_rule(static_cast<int>(n_patches), static_cast<int>(head_dim), aligned != 0,
+                            allowed, cooperative_launch, blocks_per_sm);
+  return VATTN_OK;
+}
+
+vattn_status vattn_forward_mode(const float* q, const float* k, const float* v, const float* out,
+                                int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, int* mode) {
+  g_last_error[0] = '\0';
+  if (!mode) return fail(VATTN_ERR_INVALID_ARG, "null mode pointer");
+  *mode = VATTN_MODE_NONE;
+  vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  int64_t bh = 0;
+  bool empty = false;
+  chk = check_attention_tensors(q, k, v, out, batch, n_heads, n_patches, head_dim, &bh, &empty);
+  if (chk != VATTN_OK || empty) return chk;
+  int device = 0;
+  const cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  vattn_mode m = VATTN_MODE_NONE;
+  const vattn_status st = forward_mode_on(device, q, k, v, static_cast<int>(n_patches),
+                                          static_cast<int>(head_dim), true, &m);
+  if (st == VATTN_OK) *mode = m;
+  return st;
+}
+
+int vattn_set_single_kernel(int allow) {
+  return g_single_kernel_allowed.exchange(allow != 0 ? 1 : 0);
+}
+
+int vattn_set_split_tiles(int allow) { return g_cut_allowed.exchange(allow != 0 ? 1 : 0); }
+
 const char* vattn_last_error_string(void) { return g_last_error; }
 
 int vattn_version(void) { return 100; }
@@ -1215,25 +1450,41 @@ constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(VATTN_NOALLOC_MAX_SC
 // vattn_forward_noalloc on the device shares it.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The second fixed array: the call's sync words (flags, cleared by a memset
+// on the stream at the start of each call) and the partial results of tiles
+// cut between two blocks of a balanced schedule.  A schedule whose partial
+// slots do not fit (more multiprocessors than this GPU has) runs uncut.
+constexpr size_t kNoAllocPartBytes = static_cast<size_t>(VATTN_NOALLOC_PART_BYTES);
+static __device__ __align__(256) uint8_t g_noalloc_part[kNoAllocPartBytes];
+
 std::mutex g_noalloc_mu;
 std::atomic<void*> g_noalloc_addr[kMaxDevices];
+std::atomic<void*> g_noalloc_part_addr[kMaxDevices];
 
-// Device address of g_noalloc_scratch on `device`, which must be current:
-// looked up on the first call per device, then cached.  A failed lookup is
-// not cached, so a later call tries again.
-vattn_status noalloc_scratch(int device, uint8_t** out) {
+// Device addresses of g_noalloc_scratch and g_noalloc_part on `device`,
+// which must be current: looked up on the first call per device, then
+// cached.  A failed lookup is not cached, so a later call tries again.
+vattn_status noalloc_scratch(int device, uint8_t** staging, uint8_t** sync_part) {
   if (device < 0 || device >= kMaxDevices) return fail(VATTN_ERR_CUDA, "device index %d out of range", device);
   void* addr = g_noalloc_addr[device].load(std::memory_order_acquire);
-  if (!addr) {
+  void* paddr = g_noalloc_part_addr[device].load(std::memory_order_acquire);
+  if (!addr || !paddr) {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     addr = g_noalloc_addr[device].load(std::memory_order_relaxed);
+    paddr = g_noalloc_part_addr[device].load(std::memory_order_relaxed);
     if (!addr) {
       const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
       if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the staging scratch");
       g_noalloc_addr[device].store(addr, std::memory_order_release);
     }
+    if (!paddr) {
+      const cudaError_t e = cudaGetSymbolAddress(&paddr, g_noalloc_part);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the partial-result scratch");
+      g_noalloc_part_addr[device].store(paddr, std::memory_order_release);
+    }
   }
-  *out = static_cast<uint8_t*>(addr);
+  *staging = static_cast<uint8_t*>(addr);
+  *sync_part = static_cast<uint8_t*>(paddr);
   return VATTN_OK;
 }
 
@@ -1271,12 +1522,23 @@ extern "C" vattn_status vattn_forward_noalloc(const float* q, const float* k, co
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   uint8_t* ws = nullptr;
-  const vattn_status st = noalloc_scratch(device, &ws);
+  uint8_t* wp = nullptr;
+  vattn_status st = noalloc_scratch(device, &ws, &wp);
   if (st != VATTN_OK) return st;
-  // Nothing in the scratch has to start at zero: the staging kernel writes
-  // every f16 element the attention kernel reads (padding columns included),
-  // and rows past n_patches are never read from memory (the tensor maps
-  // return zeros there).  Shapes of the direct f32 kernel use no scratch.
-  return run_forward(q, k, v, out, bh, N, D, ws, static_cast<size_t>(region),
+  ForwardPlan pl;
+  if ((st = plan_forward(device, q, k, v, bh, N, D, true, kNoAllocPartBytes, &pl)) != VATTN_OK)
+    return st;
+  // What must start at zero is cleared by the call itself: the sync words
+  // (the cut tiles' arrival counts and flags, and in the single cooperative
+  // kernel's mode the key-tile ready flags) sit at the start of the second
+  // array and run_forward clears them with a memset on the stream (no
+  // allocation).  The f16 copies of k and v are written by the attention
+  // kernel in the single kernel's mode, by the staging kernel otherwise
+  // (with q, every element the attention kernel reads, padding columns
+  // included); each cut tile's partial is written before its flag is
+  // raised.  Rows past n_patches are never read from memory (the tensor
+  // maps return zeros there).  The direct f32 kernel uses no staging copy.
+  return run_forward(pl, q, k, v, out, reinterpret_cast<uint32_t*>(wp),
+                     reinterpret_cast<float*>(wp + pl.sync_bytes), ws,
                      static_cast<cudaStream_t>(stream_ptr), device);
 }
