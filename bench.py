@@ -433,40 +433,68 @@ def run_vattn(args, workload):
     # timed alone through vattn_forward_f32q on k and v rounded to f16 once
     # beforehand (untimed), per-launch events on the same stream.
     d_pad = (D + 15) // 16 * 16
-    one_kernel = N > 128 and D <= 64 and D % 4 == 0
+    from vision_encoder_flash_gb300 import _lib
+    mode = _lib.forward_mode(*ptrs[:8])
+    one_kernel = mode in (_lib.MODE_DIRECT, _lib.MODE_SINGLE_KERNEL)
     if one_kernel:
         attn_ms = launch_ms
         n_attn = len(launch_ms)
-        kernel_what = (("vattn_fwd_kernel<2, 1, 0, 0, kInStageKV>" if N > 2048 else
+        single = mode == _lib.MODE_SINGLE_KERNEL
+        kernel_what = (("vattn_fwd_kernel<2, 1, 0, 0, kInStageKV>" if single else
                         "vattn_fwd_kernel<2, 1, 0, 0, kInF32>") +
                        " (the whole call is this one kernel; its CUDA events also hold the "
-                       "launch gap" + (" and the flag memset)" if N > 2048 else ")"))
+                       "launch gap" + (" and the flag memset)" if single else ")"))
     else:
-        k16, v16 = kd.half(), vd.half()
-        ptrs = (qd.data_ptr(), k16.data_ptr(), v16.data_ptr(), out.data_ptr(), B, H, N, D, sp)
-        for _ in range(args.warmup):
-            vef.forward_f32q_raw(*ptrs)
-        torch.cuda.synchronize(dev)
-        n_attn = max(3, min(args.steps, 1000))
-        ev16 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(n_attn)]
-        for s, e in ev16:
-            s.record(stream)
-            vef.forward_f32q_raw(*ptrs)
-            e.record(stream)
-        torch.cuda.synchronize(dev)
-        if vef.device_status() != 0:
-            raise RuntimeError("kernel reported a wait timeout")
-        attn_ms = [s.elapsed_time(e) for s, e in ev16]
-        del k16, v16
-        kernel_what = ("vattn_fwd_kernel<2, 1, 0, 0, kInF32Q> (attention with f32 q, f16 k and v; "
-                       "timed alone through vattn_forward_f32q)")
+        # two kernels: the attention kernel timed alone, on the operands the
+        # staging pass would give it (k and v rounded to f16 once beforehand,
+        # untimed): through vattn_forward_f32q where it applies (f32 q), else
+        # vattn_forward_f16 (q rounded too)
+        use_f32q = N > 128 and D <= 64 and D % 8 == 0
+        if use_f32q:
+            k16, v16 = kd.half(), vd.half()
+            aptrs = (qd.data_ptr(), k16.data_ptr(), v16.data_ptr(), out.data_ptr(), B, H, N, D, sp)
+            afn = vef.forward_f32q_raw
+            keep = (k16, v16)
+        elif D % 8 == 0:
+            q16, k16, v16 = qd.half(), kd.half(), vd.half()
+            aptrs = (q16.data_ptr(), k16.data_ptr(), v16.data_ptr(), out.data_ptr(), B, H, N, D, sp)
+            afn = vef.forward_f16_raw
+            keep = (q16, k16, v16)
+        else:
+            afn = None
+        if afn is None:
+            attn_ms = launch_ms
+            n_attn = len(launch_ms)
+            kernel_what = "the whole call (staging + attention; head_dim % 8 != 0 has no f16 entry)"
+        else:
+            for _ in range(args.warmup):
+                afn(*aptrs)
+            torch.cuda.synchronize(dev)
+            n_attn = max(3, min(args.steps, 1000))
+            ev16 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(n_attn)]
+            for s, e in ev16:
+                s.record(stream)
+                afn(*aptrs)
+                e.record(stream)
+            torch.cuda.synchronize(dev)
+            if vef.device_status() != 0:
+                raise RuntimeError("kernel reported a wait timeout")
+            attn_ms = [s.elapsed_time(e) for s, e in ev16]
+            del keep
+            kernel_what = (("vattn_fwd_kernel<2, 1, 0, 0, kInF32Q> (attention with f32 q, f16 k and v; "
+                            "timed alone through vattn_forward_f32q)") if use_f32q else
+                           "vattn_fwd_kernel (attention on f16 q, k, v; timed alone through "
+                           "vattn_forward_f16)")
     kernel_ms = max_over_ranks(sum(attn_ms) / len(attn_ms), pg, dev)
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     # the staging kernel: the rest of a call; HBM bytes read (f32 k and v)
     # and written (f16 k and v, rows padded to 16 elements)
     stage_ms = max(call_ms - kernel_ms, 1e-6)
-    stage_bytes = 0 if one_kernel else 2 * B * H * N * (4 * D + 2 * d_pad)
+    # (the staging pass rounds q too unless the attention kernel does: head_dim
+    # <= 64 with two query tiles)
+    n_staged = 2 if (d_pad <= 64 and N > 128 and D % 4 == 0) else 3
+    stage_bytes = 0 if one_kernel else n_staged * B * H * N * (4 * D + 2 * d_pad)
 
     pk, pk_src = peaks()
     peak_tf = float(pk["bf16_tflops"]) * F16_OVER_BF16_NOMINAL
@@ -687,7 +715,7 @@ def run_vattn(args, workload):
                          "achieved_gbs": stage_bytes / (stage_ms * 1e-3) / 1e9,
                          "peak_gbs": float(pk["hbm_gbs"]),
                          "frac": stage_bytes / (stage_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]),
-                         "what": "vattn_stage_kernel on k and v (f32 in, f16 out)",
+                         "what": f"vattn_stage_kernel on {'k and v' if n_staged == 2 else 'q, k and v'} (f32 in, f16 out)",
                          "how": "per-call time minus the attention kernel's time"}},
         "cpu_baseline": cpu_baseline,
         "clocks": clocks,
