@@ -561,6 +561,7 @@ def run_vattn(args, workload):
 
     # ---- the other seeded workloads (context; not the bench line)
     extras = {}
+    launch_floor = None
     if not args.no_extras:
         for idx, w in sorted(WORKLOADS.items()):
             if w.name == workload.name:
@@ -580,6 +581,7 @@ def run_vattn(args, workload):
             b.record(stream)
             torch.cuda.synchronize(dev)
             ms = a.elapsed_time(b) / reps
+            qf_ms = queue_filled_ms(torch, stream, lambda: vef.forward_raw(*xp))
             cold = cold_call_ms(torch, dev, stream, lambda: vef.forward_raw(*xp))
             c10, c50, c90 = percentiles(cold)
             wbytes = 16 * w.batch * w.n_heads * w.n_patches * w.head_dim
@@ -589,6 +591,10 @@ def run_vattn(args, workload):
                               "achieved_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
                               "frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4),
                               "l2": "hot (back-to-back, inputs may fit in L2)",
+                              "ms_queue_filled": round(qf_ms, 5),
+                              "tflops_queue_filled": round(w.flops / qf_ms / 1e9, 2),
+                              "queue_filled": "200 calls enqueued behind a 20 ms spin kernel: "
+                                              "device time per call without host gaps",
                               "cold_ms_p10_p50_p90": [round(c10, 5), round(c50, 5), round(c90, 5)],
                               "cold_tflops_p50": round(w.flops / c50 / 1e9, 2),
                               "cold": "L2 flushed (512 MB written) before each of 30 calls, "
@@ -621,6 +627,10 @@ def run_vattn(args, workload):
                 del x16
         if vef.device_status() != 0:
             raise RuntimeError("kernel reported a wait timeout")
+        launch_floor = {"us": round(1e3 * queue_filled_ms(
+            torch, stream, lambda: torch.cuda._sleep(0), reps=1000), 3),
+                        "how": "an empty kernel (torch.cuda._sleep(0)) launched 1000 times behind "
+                               "a spin kernel: device time per launch"}
 
     # ---- NeoX RoPE rows (context): the rotation fused into the staging pass
     # of a full call, and the standalone in-place rotation of q (HBM-bound:
@@ -722,6 +732,7 @@ def run_vattn(args, workload):
         "e2e": e2e,
         "gpu_launches": (1 if one_kernel else 2) * args.steps,  # (staging +) attention per step
         "other_workloads": extras,
+        "launch_floor": launch_floor,
         "variants": variants,
     }
     print(json.dumps(line), flush=True)
@@ -734,6 +745,20 @@ def percentiles(xs, qs=(10, 50, 90)):
     """Nearest-rank percentiles of a list of numbers."""
     ys = sorted(xs)
     return [ys[min(len(ys) - 1, max(0, math.ceil(q / 100 * len(ys)) - 1))] for q in qs]
+
+
+def queue_filled_ms(torch, stream, call, reps=200):
+    """Device time per call with the host far ahead of the device: a spin
+    kernel (about 20 ms) holds the stream while the host enqueues every call,
+    so the events see back-to-back calls and no host-side gaps."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(40_000_000)
+    a.record(stream)
+    for _ in range(reps):
+        call()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / reps
 
 
 def cold_call_ms(torch, dev, stream, call, reps=30):

@@ -495,7 +495,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
       ++loads;
       if (tid == 0) {
         ptx::mbar_arrive_expect_tx(slot_bar, P::kF32TileBytes);
-        ptx::tma_load_3d(slot, tm, slot_bar, 0, static_cast<int>(j) * kBN, static_cast<int>(h));
+        ptx::tma_load_3d_hint(slot, tm, slot_bar, 0, static_cast<int>(j) * kBN,
+                              static_cast<int>(h), ptx::policy_evict_first());
         *conv_ok = w.wait(slot_bar, phase, kSiteConvert) ? 1u : 0u;
       }
       ptx::named_barrier_sync(1, 128);
@@ -503,15 +504,20 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
       ptx::mbar_try_wait(slot_bar, phase);  // complete: returns at once, with acquire
       const int chunks = nr * cpr;
       uint16_t* row0 = dst + (h * N + j * kBN) * dp;
+      // the f16 rows are read back by every query block of the head: they
+      // are the last lines to leave L2 (with the f32 inputs and the output
+      // streamed evict-first, the copies are neither re-read from nor, during
+      // the call, written back to HBM)
+      const uint64_t keep = ptx::policy_evict_last();
       for (int c = tid; c < chunks; c += 128) {
         const int row = c / cpr;
         const int ch = c - row * cpr;
         const uint32_t a = slot + static_cast<uint32_t>(row * 256 + ch * 32);
         const float4 lo = ptx::ld_shared_v4(a);
         const float4 hi = ptx::ld_shared_v4(a + 16u);
-        ptx::st_global_v4(row0 + static_cast<int64_t>(row) * dp + ch * 8,
-                          ptx::pack_half2(lo.x, lo.y), ptx::pack_half2(lo.z, lo.w),
-                          ptx::pack_half2(hi.x, hi.y), ptx::pack_half2(hi.z, hi.w));
+        ptx::st_global_v4_hint(row0 + static_cast<int64_t>(row) * dp + ch * 8,
+                               ptx::pack_half2(lo.x, lo.y), ptx::pack_half2(lo.z, lo.w),
+                               ptx::pack_half2(hi.x, hi.y), ptx::pack_half2(hi.z, hi.w), keep);
       }
       // every thread has read the slot before the next TMA load refills it
       ptx::fence_proxy_async_smem();
@@ -656,6 +662,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
           ptx::prefetch_tensormap(&tm_vl);
         }
         int64_t k_issued = 0, v_issued = 0;
+        const uint64_t keep = ptx::policy_evict_last();  // K/V tiles: read by every query block
         bool ok = true;
         int g = 0;  // key tiles of this block so far
         for (int i = 0; ok && i < n_mine; ++i) {
@@ -674,8 +681,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
             if (!(ok = w.wait(bar(kBarKEmpty + st), free_par, kSiteProducerK))) break;
             ptx::mbar_arrive_expect_tx(bar(kBarKFull + st), P::kParts * tile_bytes);
             for (int kb = 0; kb < NKB; ++kb) {
-              ptx::tma_load_3d(base_s + P::kOffK + st * P::kStageStride + kb * kBoxBytes, &tm_k,
-                               bar(kBarKFull + st), kb * 64, j * kBN, bh);
+              ptx::tma_load_3d_hint(base_s + P::kOffK + st * P::kStageStride + kb * kBoxBytes,
+                                    &tm_k, bar(kBarKFull + st), kb * 64, j * kBN, bh, keep);
               if constexpr (kAcc)
                 ptx::tma_load_3d(base_s + P::kOffK + st * P::kStageStride + P::kPartBytes +
                                      kb * kBoxBytes,
@@ -685,8 +692,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
             if (!(ok = w.wait(bar(kBarVEmpty + st), free_par, kSiteProducerV))) break;
             ptx::mbar_arrive_expect_tx(bar(kBarVFull + st), P::kParts * tile_bytes);
             for (int kb = 0; kb < NKB; ++kb) {
-              ptx::tma_load_3d(base_s + P::kOffV + st * P::kStageStride + kb * kBoxBytes, &tm_v,
-                               bar(kBarVFull + st), kb * 64, j * kBN, bh);
+              ptx::tma_load_3d_hint(base_s + P::kOffV + st * P::kStageStride + kb * kBoxBytes,
+                                    &tm_v, bar(kBarVFull + st), kb * 64, j * kBN, bh, keep);
               if constexpr (kAcc)
                 ptx::tma_load_3d(base_s + P::kOffV + st * P::kStageStride + P::kPartBytes +
                                      kb * kBoxBytes,
@@ -711,8 +718,9 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
       // is ready and reloads slot t with the next tile's Q_t.
       auto load_q = [&](int i, int t) {
         ptx::mbar_arrive_expect_tx(bar(kBarF32Full + t), P::kF32TileBytes);
-        ptx::tma_load_3d(base_s + P::kOffF32 + static_cast<uint32_t>(t * P::kF32TileBytes), &tm_q,
-                         bar(kBarF32Full + t), 0, tile_row0(i) + t * kBM, tile_bh(i));
+        ptx::tma_load_3d_hint(base_s + P::kOffF32 + static_cast<uint32_t>(t * P::kF32TileBytes),
+                              &tm_q, bar(kBarF32Full + t), 0, tile_row0(i) + t * kBM, tile_bh(i),
+                              ptx::policy_evict_first());  // each q row is read once
       };
       if (lane == 0) {
         ptx::prefetch_tensormap(&tm_q);
@@ -1149,7 +1157,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&tm_o, buf, c * 16, row_base, pc_bh);
+            ptx::tma_store_3d_hint(&tm_o, buf, c * 16, row_base, pc_bh,
+                                   ptx::policy_evict_first());  // written once, not read here
             ptx::bulk_commit_group();
           }
         }
