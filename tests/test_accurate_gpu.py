@@ -22,15 +22,16 @@ Error model, with u = 2^-24 (f32 unit roundoff):
 * an output is a convex combination of v rows, so it moves by at most
   max|v - out| (~2 max|v|) times the score error;
 * the accumulator O = sum_j p_j v_j takes one tensor-core product per 16
-  keys, and its f32 accumulation does not round to nearest: measured, the
-  rel L2 error grows linearly in n_patches, as about (n_patches / 16) u
-  (4.5e-7, 1.3e-6, 3.9e-6, 1.5e-5 at n_patches 64, 256, 1024, 4100),
-  the signature of a rounding bias that adds up over the n_patches / 16
-  accumulations instead of averaging out.
+  keys, n_patches / 16 accumulations into f32.  If an accumulation does not
+  round to nearest but truncates, it loses at most one f32 ulp of the
+  running sum, 2u relative, and those losses share a sign, so they add up:
+  at most (n_patches / 16) * 2u relative over the whole sum.  (Measured, the
+  rel L2 error does grow linearly in n_patches, at about half that worst
+  case: 4.5e-7, 1.3e-6, 3.9e-6, 1.5e-5 at n_patches 64, 256, 1024, 4100.)
 
 The bars are max abs <= 5e-5 and rel L2 <= 1e-5 + (n_patches / 16) * 2u:
-the model's few 1e-6 with a tenfold margin, plus twice the accumulation
-term.  At n_patches <= 1024 that is under 2e-5, fifty times tighter than the
+the score and weight model's few 1e-6 with a tenfold margin, plus the
+worst-case truncation term of the O accumulation.  At n_patches <= 1024 that is under 2e-5, fifty times tighter than the
 f16 path's acceptance bar (3e-3, 1e-3).  A second check pins the mode
 against the f16 path itself: on the same inputs its rel L2 error is at least
 ten times smaller.

@@ -9,8 +9,7 @@ last round (or two) into one equal key range per block; every kernel mode is cov
 direct f32 kernel, the single cooperative kernel, the two-kernel mode with
 the f32-q attention kernel (q 4-byte aligned only) and with two query tiles
 sharing one P buffer (head_dim 65..96), and one query tile per block
-(head_dim 128).  Checks, on sampled rows that include every head's first and
-last row (so the cut tiles of the last rounds are among them):
+(head_dim 128).  Checks, on every output element:
 
 * acceptance against the f64 oracle (max abs 3e-3, rel L2 twice 1e-3, as for
   the other shapes outside the seeded workloads);
@@ -74,14 +73,6 @@ def run(torch_dev, q, k, v, q_offset=0):
     return out.cpu().numpy(), mode
 
 
-def sample_rows(shape, seed):
-    b, h, n, _ = shape
-    rng = np.random.default_rng(seed)
-    heads = np.arange(b * h) * n
-    return np.union1d(rng.choice(b * h * n, size=min(b * h * n, 256), replace=False),
-                      np.concatenate([heads, heads + n - 1, heads + n // 2]))
-
-
 def f16(x):
     return x.astype(np.float16).astype(np.float32)
 
@@ -106,16 +97,15 @@ def test_cut_schedule(torch_dev, shape, q_offset, mode):
     q, k, v = make_inputs(*shape, seed=seed)
     got, got_mode = run(torch_dev, q, k, v, q_offset)
     assert got_mode == mode
-    rows = sample_rows(shape, seed)
-    d = shape[3]
-    sel = got.reshape(-1, d)[rows].astype(np.float64)
+    # every output element against the oracle
+    sel = got.astype(np.float64)
     assert np.all(np.isfinite(sel))
-    ref = oracle.rows(q, k, v, rows)
+    ref = oracle.forward(q, k, v)
     mx = float(np.abs(sel - ref).max())
     rel = float(np.linalg.norm(sel - ref) / np.linalg.norm(ref))
     assert mx <= MAX_ABS and rel <= 2 * MAX_REL_L2, f"{shape}: max abs {mx:.3e}, rel L2 {rel:.3e}"
     # kernel arithmetic against the oracle on the f16-rounded inputs
-    ref16 = oracle.rows(f16(q), f16(k), f16(v), rows)
+    ref16 = oracle.forward(f16(q), f16(k), f16(v))
     n = shape[2]
     bound = (2.0 ** -11 + n * 2.0 ** -24) * float(np.abs(f16(v)).max()) + 1e-5
     mx16 = float(np.abs(sel - ref16).max())
