@@ -412,25 +412,41 @@ vattn_status vattn_forward_mode_for(int64_t batch, int64_t n_heads, int64_t n_pa
 int vattn_set_single_kernel(int allow);
 
 /*
- * vattn_set_split_tiles -- allow (allow != 0) or forbid (allow == 0, the
- * default) cut work tiles, process-wide.  The attention kernel is
+ * vattn_set_split_tiles -- cut work tiles where it pays (allow == 1, the
+ * default), never (allow <= 0), or wherever it shortens the busiest block
+ * (allow >= 2, for tests and measurements), process-wide.  The attention kernel is
  * persistent (one thread block per multiprocessor); when the work tiles
  * (128 or 256 query rows of one head) do not divide evenly over the blocks,
- * vattn_forward and vattn_forward_noalloc cut the tiles of the last round by
- * key range, one equal share per block, and the two parts of a cut tile are
- * combined by the log-sum-exp rule (the shader's rescale of (m, l, o)).  The
- * result is the same attention, but the rounding of a cut tile's rows then
- * depends on how the call's work was shared out, i.e. on the other heads in
- * the call.  Forbidden, every tile runs whole in one block: each output row
- * depends only on its own head's inputs (bit-identical whatever else the
- * call holds, as in vattn_forward_f16 / _f32q / _host, which never cut),
- * at the price of a partial last round.  Measured on GB300, the pieces'
- * extra prologues and merges cost about what the balanced round saves, so
- * cut tiles are off unless allowed here.  Returns the previous setting.  Not
- * synchronised with calls in flight on other host threads: set it before
- * them.  The shader has no counterpart (one workgroup per block of rows).
+ * vattn_forward and vattn_forward_noalloc may cut the tiles of the last
+ * round(s) by key range, one equal share per block, and the two parts of a
+ * cut tile are combined by the log-sum-exp rule (the shader's rescale of
+ * (m, l, o)).  They do so only where it pays, measured on GB300: tiles of at
+ * least 16 key tiles (2048 patches) and a busiest block shorter by at least
+ * 7 key tiles (for example 8 x 16 heads x 2304 patches, or 2 x 16 heads x
+ * 4096 patches, 8 % faster).  The result is the same attention, but the
+ * rounding of a cut tile's rows then depends on how the call's work was
+ * shared out, i.e. on the other heads in the call.  Forbidden, every tile
+ * runs whole in one block: each output row depends only on its own head's
+ * inputs (bit-identical whatever else the call holds, as in
+ * vattn_forward_f16 / _f32q / _host, which never cut), at the price of a
+ * partial last round.  Not synchronised with calls in flight on other host
+ * threads: set it before them.  The shader
+ * has no counterpart (one workgroup per block of rows).  Returns the
+ * previous setting (0, 1 or 2).
  */
 int vattn_set_split_tiles(int allow);
+
+/*
+ * vattn_cut_plan_for -- host-only query: whether vattn_forward would cut
+ * work tiles (see vattn_set_split_tiles) for q, k, v of these sizes on a
+ * device whose persistent grid has n_blocks thread blocks (its
+ * multiprocessor count), under the current process-wide setting.  *cut: 1
+ * or 0 (0 for an empty problem).  No GPU is touched.  Errors: a null `cut`,
+ * n_blocks < 1 or sizes outside the limits of vattn_forward (the same
+ * status as vattn_forward for those).  The shader has no counterpart.
+ */
+vattn_status vattn_cut_plan_for(int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, int n_blocks, int* cut);
 
 /*
  * vattn_device_status -- reads and clears the kernel-side error word of the

@@ -27,7 +27,7 @@ def test_exports_every_declared_symbol(lib):
                           "vattn_device_status", "vattn_status_string",
                           "vattn_last_error_string", "vattn_version",
                           "vattn_forward_mode", "vattn_forward_mode_for",
-                          "vattn_set_single_kernel", "vattn_set_split_tiles"}
+                          "vattn_set_single_kernel", "vattn_set_split_tiles", "vattn_cut_plan_for"}
     for name in names:
         assert hasattr(lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.lib_path()], capture_output=True,

@@ -3,9 +3,9 @@ two thread blocks, the two parts merged by the log-sum-exp rule (the rescale
 of (m, l, o) by the larger maximum that the shader applies per key tile).
 
 Each shape below has more work tiles than the GPU has multiprocessors and a
-partial last round, so vattn_forward, with cut tiles allowed
-(vattn_set_split_tiles(1); they are off by default), cuts the tiles of the
-last round (or two) into one equal key range per block; every kernel mode is covered: the
+partial last round, so vattn_forward, with cutting forced
+(vattn_set_split_tiles(2); by default it cuts only where that pays), cuts
+the tiles of the last round (or two) into one equal key range per block; every kernel mode is covered: the
 direct f32 kernel, the single cooperative kernel, the two-kernel mode with
 the f32-q attention kernel (q 4-byte aligned only) and with two query tiles
 sharing one P buffer (head_dim 65..96), and one query tile per block
@@ -18,8 +18,10 @@ sharing one P buffer (head_dim 65..96), and one query tile per block
   (vattn_set_split_tiles(0)): the parts of a cut tile take their own maxima,
   so their f16 softmax weights round differently, within the same bound.
 
-Cut tiles are off by default because, on this kernel, the pieces' extra
-prologues and merges cost about what the balanced last round saves."""
+By default tiles are cut only where that pays: the pieces' extra prologues
+and merges cost about the time of 5 to 10 key tiles per call, so only long
+tiles (at least 16 key tiles) with a busiest block shorter by at least 7 key
+tiles are cut (the rule is checked on the host in test_mode_rule.py)."""
 import numpy as np
 import pytest
 
@@ -48,10 +50,12 @@ def torch_dev():
 
 
 @pytest.fixture(autouse=True)
-def cutting_allowed(torch_dev):
-    """Cut tiles are off by default (vattn_set_split_tiles); these tests turn
-    them on and restore the previous setting."""
-    prev = _lib.set_split_tiles(True)
+def cutting_forced(torch_dev):
+    """By default tiles are cut only where it pays (long tiles, a clearly
+    shorter busiest block); these tests cut wherever the schedule allows
+    (vattn_set_split_tiles(2)), so that every kernel mode runs cut tiles,
+    and restore the previous setting."""
+    prev = _lib.set_split_tiles(2)
     yield
     _lib.set_split_tiles(prev)
 

@@ -77,3 +77,44 @@ def test_device_query_checks_arguments_before_any_cuda_call(lib):
     assert e.value.status == 1
     # an empty problem needs no device either
     assert _lib.forward_mode(fake, fake, fake, fake + 2 ** 30, 0, 1, 2, 4) == _lib.MODE_NONE
+
+
+# The cut rule (vattn_set_split_tiles, vattn_cut_plan_for): on a 152-block
+# grid, with the default setting, tiles are cut only where the measured
+# saving exceeds the pieces' cost -- long tiles (>= 16 key tiles) and a
+# busiest block shorter by >= 7 key tiles.
+@pytest.mark.parametrize("shape,cut", [
+    ((8, 16, 2304, 64), True),    # 1152 tiles of 18 key tiles: 144 -> 137 per block
+    ((2, 16, 4096, 64), True),    # 512 tiles of 32: 128 -> 108
+    ((1, 16, 4100, 72), False),   # 272 tiles of 33: saves 6
+    ((4, 16, 1024, 64), False),   # tiles of 8 key tiles: too short
+    ((2, 40, 2176, 64), False),   # 720 tiles of 17: saves 4
+    ((1, 16, 2304, 64), False),   # 144 tiles: one round, nothing to balance
+    ((2, 30, 2100, 20), True),    # 540 tiles of 17: 68 -> 61
+])
+def test_cut_rule_default(lib, shape, cut):
+    prev = _lib.set_split_tiles(1)
+    try:
+        assert _lib.cut_plan_for(*shape, 152) == cut
+    finally:
+        _lib.set_split_tiles(prev)
+
+
+def test_cut_rule_forced_and_forbidden(lib):
+    prev = _lib.set_split_tiles(2)
+    try:
+        assert _lib.cut_plan_for(4, 16, 1024, 64, 152)       # forced: short tiles cut too
+        assert not _lib.cut_plan_for(1, 16, 2304, 64, 152)   # nothing to balance
+        assert _lib.set_split_tiles(0) == 2
+        assert not _lib.cut_plan_for(8, 16, 2304, 64, 152)
+        assert not _lib.cut_plan_for(2, 16, 4096, 64, 152)
+        assert _lib.set_split_tiles(1) == 0
+        assert _lib.cut_plan_for(8, 16, 2304, 64, 152)
+    finally:
+        _lib.set_split_tiles(prev)
+
+
+def test_cut_rule_argument_errors(lib):
+    with pytest.raises(vef.VattnError):
+        _lib.cut_plan_for(8, 16, 2304, 64, 0)
+    assert not _lib.cut_plan_for(0, 16, 2304, 64, 152)       # empty problem

@@ -67,6 +67,8 @@ def load_library():
     lib.vattn_set_single_kernel.restype = ctypes.c_int
     lib.vattn_set_split_tiles.argtypes = [ctypes.c_int]
     lib.vattn_set_split_tiles.restype = ctypes.c_int
+    lib.vattn_cut_plan_for.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    lib.vattn_cut_plan_for.restype = ctypes.c_int
     lib.vattn_selftest_wait_timeout.argtypes = [vp]
     lib.vattn_selftest_wait_timeout.restype = ctypes.c_int
     lib.vattn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -221,10 +223,20 @@ def set_single_kernel(allow: bool) -> bool:
     return bool(load_library().vattn_set_single_kernel(1 if allow else 0))
 
 
-def set_split_tiles(allow: bool) -> bool:
-    """Allow or forbid cut work tiles (balanced last round) process-wide;
-    returns the previous setting."""
-    return bool(load_library().vattn_set_split_tiles(1 if allow else 0))
+def set_split_tiles(allow) -> int:
+    """Cut work tiles (balanced last round), process-wide: 0 / False never,
+    1 / True where it pays (the default), 2 wherever it shortens the busiest
+    block; returns the previous setting (0, 1 or 2)."""
+    return int(load_library().vattn_set_split_tiles(int(allow)))
+
+
+def cut_plan_for(batch: int, n_heads: int, n_patches: int, head_dim: int, n_blocks: int) -> bool:
+    """Whether vattn_forward would cut work tiles for these sizes on a grid of
+    n_blocks thread blocks, under the current setting (host only)."""
+    cut = ctypes.c_int(0)
+    _check(load_library().vattn_cut_plan_for(batch, n_heads, n_patches, head_dim, n_blocks,
+                                              ctypes.byref(cut)))
+    return cut.value != 0
 
 
 def selftest_wait_timeout(stream: int = 0) -> None:

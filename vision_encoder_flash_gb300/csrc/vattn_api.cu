@@ -187,10 +187,17 @@ vattn_status sm_count(int device, int* out) {
 // key tiles on `grid` blocks (the kernel's Sched).  Whole tiles in rounds;
 // when the rounds leave a last, partial round (n_tiles % grid != 0) and
 // cutting is allowed, the last one or two rounds' tiles are instead cut by
-// key ranges into one equal share per block -- provided that shortens the
-// busiest block by at least two key tiles, which pays for the merge of the
-// cut tiles.  Each share holds at least T key tiles (the tail has at least
-// `grid` tiles), so a tile is cut at most once.
+// key ranges into one equal share per block -- provided the tiles are long
+// (at least kCutMinKeyTiles key tiles) and the cut shortens the busiest
+// block by at least kCutMinSaving key tiles.  The pieces' extra prologues
+// and the merges of the cut tiles cost, measured on GB300, the time of 5 to
+// 10 key tiles per call (8 x 16 heads: +22 % at 1024 patches, tiles of 8 key
+// tiles, saving 2; +2 % at 16 x 4100, saving 6; -1.3 % at 2304 patches,
+// saving 7; 2 x 16 heads at 4096 patches: -8.2 %, saving 20).  Each share
+// holds at least T key tiles (the tail has at least `grid` tiles), so a tile
+// is cut at most once.
+constexpr int kCutMinKeyTiles = 16;
+constexpr int kCutMinSaving = 7;
 struct Schedule {
   int rounds = 0;
   int extra = 0;
@@ -198,18 +205,20 @@ struct Schedule {
   bool cut = false;
 };
 
-// Process-wide switch of vattn_set_split_tiles (off by default).
-std::atomic<int> g_cut_allowed{0};
+// Process-wide switch of vattn_set_split_tiles: 0 never cut, 1 cut where it
+// pays (the default), 2 cut wherever it shortens the busiest block.
+std::atomic<int> g_cut_allowed{1};
 
-Schedule make_schedule(long long n_tiles, int T, int grid, bool allow_cut) {
+Schedule make_schedule(long long n_tiles, int T, int grid, int cut_mode) {
   Schedule s;
   s.rounds = static_cast<int>(n_tiles / grid);
   s.extra = static_cast<int>(n_tiles % grid);
-  if (!allow_cut || s.extra == 0 || grid < 2) return s;
+  if (cut_mode == 0 || s.extra == 0 || grid < 2) return s;
   const int r = n_tiles >= 2LL * grid ? s.rounds - 1 : 0;
   const long long tail = (n_tiles - static_cast<long long>(r) * grid) * T;
   const long long busiest_cut = static_cast<long long>(r) * T + (tail + grid - 1) / grid;
   const long long busiest_whole = static_cast<long long>(s.rounds + 1) * T;
+  if (cut_mode == 1 && (T < kCutMinKeyTiles || busiest_cut + kCutMinSaving > busiest_whole)) return s;
   if (busiest_cut + 2 > busiest_whole) return s;
   s.rounds = r;
   s.extra = 0;
@@ -659,8 +668,8 @@ vattn_status plan_forward(int device, const float* q, const float* k, const floa
   const size_t cut_need = round256((cut_words + pl.flag_words) * sizeof(uint32_t)) +
                           round256(static_cast<size_t>(pl.grid - 1) * slot_bytes);
   pl.sched = make_schedule(pl.n_tiles, pl.T, pl.grid,
-                           cut_need <= max_sync_part_bytes &&
-                               g_cut_allowed.load(std::memory_order_relaxed) != 0);
+                           cut_need <= max_sync_part_bytes
+                               ? g_cut_allowed.load(std::memory_order_relaxed) : 0);
   if (pl.sched.cut) {
     pl.cut_words = cut_words;
     pl.part_bytes = round256(static_cast<size_t>(pl.grid - 1) * slot_bytes);
@@ -1399,6 +1408,29 @@ vattn_status vattn_forward_mode_for(int64_t batch, int64_t n_heads, int64_t n_pa
   return VATTN_OK;
 }
 
+vattn_status vattn_cut_plan_for(int64_t batch, int64_t n_heads, int64_t n_patches,
+                                int64_t head_dim, int n_blocks, int* cut) {
+  g_last_error[0] = '\0';
+  if (!cut) return fail(VATTN_ERR_INVALID_ARG, "null cut pointer");
+  *cut = 0;
+  if (n_blocks < 1) return fail(VATTN_ERR_INVALID_ARG, "n_blocks must be at least 1");
+  const vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
+  if (chk != VATTN_OK) return chk;
+  if (batch != 0 && n_heads > INT64_MAX / batch)
+    return fail(VATTN_ERR_UNSUPPORTED, "batch * n_heads overflows");
+  if (batch * n_heads == 0 || n_patches == 0) return VATTN_OK;
+  if (n_patches > INT32_MAX || batch * n_heads > INT32_MAX)
+    return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
+  const int N = static_cast<int>(n_patches);
+  const int d_pad = (static_cast<int>(head_dim) + 15) & ~15;
+  const int nq = query_tiles(N, d_pad);
+  const long long n_tiles = batch * n_heads * ((N + vattn::kBM * nq - 1) / (vattn::kBM * nq));
+  const int T = (N + vattn::kBN - 1) / vattn::kBN;
+  const int grid = static_cast<int>(n_tiles < n_blocks ? n_tiles : n_blocks);
+  *cut = make_schedule(n_tiles, T, grid, g_cut_allowed.load(std::memory_order_relaxed)).cut ? 1 : 0;
+  return VATTN_OK;
+}
+
 vattn_status vattn_forward_mode(const float* q, const float* k, const float* v, const float* out,
                                 int64_t batch, int64_t n_heads, int64_t n_patches,
                                 int64_t head_dim, int* mode) {
@@ -1425,7 +1457,9 @@ int vattn_set_single_kernel(int allow) {
   return g_single_kernel_allowed.exchange(allow != 0 ? 1 : 0);
 }
 
-int vattn_set_split_tiles(int allow) { return g_cut_allowed.exchange(allow != 0 ? 1 : 0); }
+int vattn_set_split_tiles(int allow) {
+  return g_cut_allowed.exchange(allow <= 0 ? 0 : (allow == 1 ? 1 : 2));
+}
 
 const char* vattn_last_error_string(void) { return g_last_error; }
 
