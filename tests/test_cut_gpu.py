@@ -145,3 +145,28 @@ def test_forbidding_cuts_makes_rows_independent_of_the_batch(torch_dev):
     finally:
         _lib.set_split_tiles(prev)
     assert np.array_equal(full[:, 37:38].view(np.uint32), one.view(np.uint32))
+
+
+@pytest.mark.parametrize("shape,mode", [
+    ((2, 16, 4096, 64), _lib.MODE_SINGLE_KERNEL),   # 512 tiles of 32 key tiles
+    ((4, 20, 2048, 64), _lib.MODE_DIRECT),          # 640 tiles of 16 key tiles
+])
+def test_default_rule_cuts_and_matches_the_oracle(torch_dev, shape, mode):
+    """Shapes that the default setting itself cuts (vattn_set_split_tiles(1)),
+    every output element against the oracle."""
+    torch, dev = torch_dev
+    prev = _lib.set_split_tiles(1)
+    try:
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        assert _lib.cut_plan_for(*shape, n_sm)
+        q, k, v = make_inputs(*shape, seed=9400 + shape[2])
+        got, got_mode = run(torch_dev, q, k, v)
+    finally:
+        _lib.set_split_tiles(prev)
+    assert got_mode == mode
+    ref = oracle.forward(q, k, v)
+    sel = got.astype(np.float64)
+    assert np.all(np.isfinite(sel))
+    mx = float(np.abs(sel - ref).max())
+    rel = float(np.linalg.norm(sel - ref) / np.linalg.norm(ref))
+    assert mx <= MAX_ABS and rel <= 2 * MAX_REL_L2, f"{shape}: max abs {mx:.3e}, rel L2 {rel:.3e}"
