@@ -56,7 +56,10 @@ typedef enum {
  *
  * The call is asynchronous: it validates arguments, launches its kernels on
  * `stream` and returns; the result is ready when the stream reaches that
- * point.  Three paths, the same f16 rounding and bit-identical results:
+ * point.  Three paths, the same f16 rounding and, for the same work
+ * schedule, bit-identical results (where the last round of work tiles is
+ * cut between blocks, see vattn_set_split_tiles, a row's last bits depend on
+ * that schedule):
  *   - 128 < n_patches <= 2048, head_dim 33..64 and a multiple of 4, q, k, v
  *     16-byte aligned: one kernel that reads the f32 tiles and rounds them
  *     to f16 in shared memory; nothing is allocated;
@@ -269,9 +272,10 @@ vattn_status vattn_conv1d_step(const float* input, float* buffer, const float* w
  * host-to-device copies of its q, k and v, the kernels of vattn_forward (the
  * direct f32 kernel, else the staging kernel and the attention kernel: not
  * the single cooperative kernel), and the device-to-host copy of its output,
- * so that the copies of one chunk overlap the kernels of the next.  The
- * result is bit-identical to vattn_forward on the same values (the same
- * rounding and arithmetic per head).
+ * so that the copies of one chunk overlap the kernels of the next.  Tiles
+ * are never cut here, so the result is bit-identical to vattn_forward on
+ * the same values with cutting forbidden (vattn_set_split_tiles(0)); with
+ * the default setting, to within the rounding of the cut tiles' merge.
  *
  * q, k, v, out: HOST pointers to contiguous f32 [batch, n_heads, n_patches,
  *   head_dim], head-major, 4-byte aligned; out must not overlap q, k or v.
@@ -349,8 +353,9 @@ vattn_status vattn_forward_noalloc(const float* q, const float* k, const float* 
                                    int64_t head_dim, void* stream);
 
 /*
- * Kernel modes of vattn_forward (all give bit-identical results: the same
- * f16 rounding and the same tensor-core arithmetic).  The shader has one
+ * Kernel modes of vattn_forward (all give bit-identical results for the
+ * same work schedule: the same f16 rounding and the same tensor-core
+ * arithmetic).  The shader has one
  * compute pass per call; these are this library's ways of scheduling it.
  *   VATTN_MODE_NONE           empty problem: nothing is launched;
  *   VATTN_MODE_DIRECT         one kernel on the f32 tiles (q, k, v rounded
