@@ -60,9 +60,10 @@ typedef enum {
  * schedule, bit-identical results (where the last round of work tiles is
  * cut between blocks, see vattn_set_split_tiles, a row's last bits depend on
  * that schedule):
- *   - 128 < n_patches <= 2048, head_dim 33..64 and a multiple of 4, q, k, v
- *     16-byte aligned: one kernel that reads the f32 tiles and rounds them
- *     to f16 in shared memory; nothing is allocated;
+ *   - 128 < n_patches <= 2048 with head_dim 33..64, or n_patches <= 128
+ *     with head_dim <= 64, head_dim a multiple of 4, q, k, v 16-byte
+ *     aligned: one kernel that reads the f32 tiles and rounds them to f16
+ *     in shared memory; nothing is allocated;
  *   - n_patches > 2048 with head_dim <= 64 and a multiple of 4 and q, k, v
  *     16-byte aligned (also head_dim <= 32 from 129 patches on): a memset
  *     and one cooperative kernel that writes the f16 copies of k and v

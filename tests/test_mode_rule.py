@@ -29,7 +29,9 @@ def lib():
     ((4, 16, 2049, 64), 1, SINGLE),
     ((1, 16, 4100, 72), 1, TWO),         # head_dim past 64
     ((1, 16, 4100, 62), 1, TWO),         # head_dim not a multiple of 4
-    ((1, 2, 64, 32), 1, TWO),            # one query tile (<= 128 patches)
+    ((1, 2, 64, 32), 1, DIRECT),         # up to 128 patches: one launch, the direct kernel
+    ((1, 2, 64, 30), 1, TWO),            # head_dim not a multiple of 4
+    ((1, 2, 128, 64), 1, DIRECT),
     ((1, 2, 129, 32), 1, SINGLE),        # head_dim <= 32 takes the single kernel from 129 patches
     ((1, 16, 256, 64), 1, DIRECT),
     ((2, 2, 130, 128), 1, TWO),

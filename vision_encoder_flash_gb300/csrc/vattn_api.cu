@@ -321,7 +321,9 @@ int query_tiles(int n_patches, int d_pad) {
 
 // f32 inputs the attention kernel reads directly (its converter warps round
 // them to f16 in shared memory, no staging pass): two query tiles, head_dim
-// 33..64 and a multiple of 4, 16-byte aligned q, k, v, and n_patches <= 2048.
+// 33..64 and a multiple of 4, 16-byte aligned q, k, v, and n_patches <= 2048;
+// and any head_dim <= 64 (a multiple of 4) up to 128 patches, where one
+// launch instead of two is what counts.
 // Each block rounds the K and V tiles of its own query rows, so a head's
 // keys are rounded once per 256 query rows and the shared-memory traffic
 // grows with n_patches; measured on GB300 (8 x 16 heads, head_dim 64) the
@@ -330,7 +332,12 @@ int query_tiles(int n_patches, int d_pad) {
 // cheaper (head_dim 32 at 1024 patches: 0.96x), so they keep the two passes.
 bool direct_shape(int N, int D) {
   const int d_pad = (D + 15) & ~15;
-  return d_pad <= 64 && D > 32 && D % 4 == 0 && N <= 2048 && query_tiles(N, d_pad) == 2;
+  if (d_pad > 64 || D % 4 != 0) return false;
+  // up to 128 patches (one work tile per head, one key tile): the direct
+  // kernel's second query tile reads as zero rows and stores nothing, and
+  // the call is one launch instead of a staging pass and the attention kernel
+  if (N <= 128) return true;
+  return D > 32 && N <= 2048 && query_tiles(N, d_pad) == 2;
 }
 
 bool aligned16(const void* q, const void* k, const void* v) {
