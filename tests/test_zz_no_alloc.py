@@ -86,6 +86,10 @@ def assert_close(got, ref, what):
     # two kernels on one query tile (64 patches, head_dim not a multiple of
     # 4), then the single kernel at head_dim 20 with a ragged last key tile
     ((1, 2, 64, 30), (2, 8, 2500, 20)),
+    # the single kernel with the last round's tiles cut by key range (the
+    # default rule cuts 256 tiles of 32 key tiles on a 152-block grid): the
+    # cut tiles' partial results in the second array; then a small call
+    ((1, 16, 4096, 64), (1, 3, 200, 38)),
 ])
 def test_noalloc_matches_forward_two_calls_in_a_row(torch_dev, first, second):
     torch, dev = torch_dev
