@@ -104,8 +104,10 @@ PAIR = [(d, n) for d in (8, 20, 32, 48, 60, 64) for n in (257, 511, 512, 513, 10
 
 
 # head_dim 65..96 with more than one query tile: two query tiles that share
-# one P buffer, two column blocks, several work tiles per head, ragged ends
-SHARED_P = [(d, n) for d in (65, 70, 88, 96) for n in (129, 257, 511, 1025)]
+# one P buffer, two column blocks, several work tiles per head; n_patches
+# with a whole number of key tiles (256), one key in the last one (257,
+# 1025) and ragged ends
+SHARED_P = [(d, n) for d in (65, 70, 80, 88, 96) for n in (129, 192, 256, 257, 511, 1025, 1057)]
 
 
 @pytest.mark.parametrize("d,n", SHARED_P)
@@ -143,11 +145,13 @@ def test_workload_5_full(torch_dev):
     print(f"{WORKLOADS[5].name}: max abs {mx:.3e} rel L2 {rel:.3e}")
 
 
+@pytest.mark.parametrize("D", [64, 80])
 @pytest.mark.parametrize("order", ["increasing", "decreasing", "shuffled"])
-def test_running_max_rescale_paths(torch_dev, order):
+def test_running_max_rescale_paths(torch_dev, order, D):
     # scores 40*j/512 (exact in f16): increasing order raises the row max by
-    # 10 (14.4 in log2 units) on every key tile, forcing an O rescale each time
-    N, D = 1024, 64
+    # 10 (14.4 in log2 units) on every key tile, forcing an O rescale each
+    # time; head_dim 80 takes the shared-P kernel
+    N = 1024
     j = np.arange(N)
     if order == "decreasing":
         j = j[::-1]
