@@ -473,6 +473,11 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
     const int tid = static_cast<int>(threadIdx.x) - 128 * (1 + NQ);
     const int dp = p.d_pad;
     const int cpr = dp >> 3;  // 8-column chunks per f16 row
+    // chunk c = row * cpr + ch of a tile, walked as c = tid, tid + 128, ...
+    // without a division per chunk: 128 chunks ahead is row_step rows and
+    // ch_step chunks further on
+    const int row_first = tid / cpr, ch_first = tid - row_first * cpr;
+    const int row_step = 128 / cpr, ch_step = 128 - row_step * cpr;
     const int64_t n_bh = p.n_tiles / p.n_qblocks;
     const int64_t n_jobs = n_bh * T;
     const int64_t grid = gridDim.x;
@@ -502,44 +507,48 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
       ptx::named_barrier_sync(1, 128);
       if (*conv_ok == 0u) return false;
       ptx::mbar_try_wait(slot_bar, phase);  // complete: returns at once, with acquire
-      const int chunks = nr * cpr;
       uint16_t* row0 = dst + (h * N + j * kBN) * dp;
       // the f16 rows are read back by every query block of the head: they
       // are the last lines to leave L2 (with the f32 inputs and the output
       // streamed evict-first, the copies are neither re-read from nor, during
       // the call, written back to HBM)
       const uint64_t keep = ptx::policy_evict_last();
-      for (int c = tid; c < chunks; c += 128) {
-        const int row = c / cpr;
-        const int ch = c - row * cpr;
+      for (int row = row_first, ch = ch_first; row < nr;) {
         const uint32_t a = slot + static_cast<uint32_t>(row * 256 + ch * 32);
         const float4 lo = ptx::ld_shared_v4(a);
         const float4 hi = ptx::ld_shared_v4(a + 16u);
         ptx::st_global_v4_hint(row0 + static_cast<int64_t>(row) * dp + ch * 8,
                                ptx::pack_half2(lo.x, lo.y), ptx::pack_half2(lo.z, lo.w),
                                ptx::pack_half2(hi.x, hi.y), ptx::pack_half2(hi.z, hi.w), keep);
+        row += row_step;
+        ch += ch_step;
+        if (ch >= cpr) {
+          ch -= cpr;
+          ++row;
+        }
       }
       // every thread has read the slot before the next TMA load refills it
       ptx::fence_proxy_async_smem();
       ptx::named_barrier_sync(1, 128);
       return true;
     };
+    // The rounds of the job sequence: round r holds the heads [h0, h1) (h0
+    // = ceil(r * grid / nqb)), T jobs each, from job base_job on.  A block's
+    // jobs increase, so the round is advanced, not searched, per job.
+    int64_t r = 0, base_job = 0, h0 = 0;
+    int64_t h1 = (grid + nqb - 1) / nqb < n_bh ? (grid + nqb - 1) / nqb : n_bh;
     for (int64_t s = blockIdx.x; ok && s < n_jobs; s += grid) {
       // (bh, j) of job s
-      int64_t base_job = 0, h = 0, j = 0;
-      for (int64_t r = 0;; ++r) {
-        const int64_t h0 = (r * grid + nqb - 1) / nqb;
-        int64_t h1 = ((r + 1) * grid + nqb - 1) / nqb;
+      while (s >= base_job + (h1 - h0) * T) {
+        base_job += (h1 - h0) * T;
+        ++r;
+        h0 = h1;
+        h1 = ((r + 1) * grid + nqb - 1) / nqb;
         if (h1 > n_bh) h1 = n_bh;
-        const int64_t cnt = (h1 - h0) * T;
-        if (s < base_job + cnt) {
-          const int64_t o = s - base_job;
-          j = o / (h1 - h0);
-          h = h0 + (o - j * (h1 - h0));
-          break;
-        }
-        base_job += cnt;
       }
+      const int64_t o = s - base_job;
+      const int64_t j = o / (h1 - h0);
+      const int64_t h = h0 + (o - j * (h1 - h0));
       const int nr = (N - static_cast<int>(j) * kBN) < kBN ? (N - static_cast<int>(j) * kBN) : kBN;
       if (!(ok = stage(&tm_kl, p.k16, h, j, nr))) break;
       if (!(ok = stage(&tm_vl, p.v16, h, j, nr))) break;
