@@ -427,7 +427,7 @@ def run_vattn(args, workload):
 
     # ---- the dominant kernel alone.  With head_dim <= 64 (a multiple of 4)
     # and more than 128 patches a step is one attention kernel (which rounds
-    # q, k and v to f16 itself; past 2048 patches after clearing its key-tile
+    # q, k and v to f16 itself; in the single kernel's mode after clearing its key-tile
     # flags with a memset), so the step's own CUDA events time it.  Otherwise
     # a step is the staging kernel and then the attention kernel; that one is
     # timed alone through vattn_forward_f32q on k and v rounded to f16 once

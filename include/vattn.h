@@ -60,15 +60,17 @@ typedef enum {
  * schedule, bit-identical results (where the last round of work tiles is
  * cut between blocks, see vattn_set_split_tiles, a row's last bits depend on
  * that schedule):
- *   - 128 < n_patches <= 2048 with head_dim 33..64, or n_patches <= 128
- *     with head_dim <= 64, head_dim a multiple of 4, q, k, v 16-byte
- *     aligned: one kernel that reads the f32 tiles and rounds them to f16
- *     in shared memory; nothing is allocated;
- *   - n_patches > 2048 with head_dim <= 64 and a multiple of 4 and q, k, v
- *     16-byte aligned (also head_dim <= 32 from 129 patches on): a memset
- *     and one cooperative kernel that writes the f16 copies of k and v
- *     itself, each key tile once, while its blocks compute (a block reads a
- *     key tile once the block that wrote it has set the tile's flag), and
+ *   - 128 < n_patches <= 1536 with head_dim 33..64, or up to 2048 patches
+ *     while the work tiles (batch*n_heads * ceil(n_patches / 256)) fill at
+ *     most two rounds of the multiprocessors, or n_patches <= 128 with
+ *     head_dim <= 64; head_dim a multiple of 4, q, k, v 16-byte aligned:
+ *     one kernel that reads the f32 tiles and rounds them to f16 in shared
+ *     memory; nothing is allocated;
+ *   - otherwise, with head_dim <= 64 and a multiple of 4 and q, k, v
+ *     16-byte aligned and more than 128 patches: a memset and one
+ *     cooperative kernel that writes the f16 copies of k and v itself,
+ *     each key tile once, while its blocks compute (a block reads a key
+ *     tile once the block that wrote it has set the tile's flag), and
  *     rounds q itself;
  *   - otherwise two kernels (the f16 staging of q, k and v, then the
  *     attention kernel; the attention kernel rounds q itself when head_dim
@@ -394,15 +396,17 @@ vattn_status vattn_forward_mode(const float* q, const float* k, const float* v, 
  * device facts passed in instead of read from a device: aligned = q, k and
  * v are all 16-byte aligned; cooperative_launch = the device attribute
  * cudaDevAttrCooperativeLaunch; blocks_per_sm = resident blocks per
- * multiprocessor of the single cooperative kernel (0 when it does not fit).
- * The single kernel is taken only when cooperative_launch != 0,
- * blocks_per_sm >= 1 and vattn_set_single_kernel has not forbidden it.
- * Pure host function (no CUDA call).  Sizes are checked as in
- * vattn_forward; *mode = VATTN_MODE_NONE for an empty problem.
+ * multiprocessor of the single cooperative kernel (0 when it does not fit);
+ * n_sms = the device's multiprocessors (>= 1; VATTN_ERR_INVALID_ARG
+ * otherwise), the size of the persistent grid.  The single kernel is taken
+ * only when cooperative_launch != 0, blocks_per_sm >= 1 and
+ * vattn_set_single_kernel has not forbidden it.  Pure host function (no
+ * CUDA call).  Sizes are checked as in vattn_forward; *mode =
+ * VATTN_MODE_NONE for an empty problem.
  */
 vattn_status vattn_forward_mode_for(int64_t batch, int64_t n_heads, int64_t n_patches,
                                     int64_t head_dim, int aligned, int cooperative_launch,
-                                    int blocks_per_sm, int* mode);
+                                    int blocks_per_sm, int n_sms, int* mode);
 
 /*
  * vattn_set_single_kernel -- allow (allow != 0, the default) or forbid

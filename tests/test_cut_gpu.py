@@ -149,7 +149,8 @@ def test_forbidding_cuts_makes_rows_independent_of_the_batch(torch_dev):
 
 @pytest.mark.parametrize("shape,mode", [
     ((2, 16, 4096, 64), _lib.MODE_SINGLE_KERNEL),   # 512 tiles of 32 key tiles
-    ((4, 20, 2048, 64), _lib.MODE_DIRECT),          # 640 tiles of 16 key tiles
+    ((4, 20, 2048, 64), _lib.MODE_SINGLE_KERNEL),   # 640 tiles of 16 key tiles
+    ((1, 20, 2048, 64), _lib.MODE_DIRECT),          # 160 tiles of 16: 32 -> 17 per block
 ])
 def test_default_rule_cuts_and_matches_the_oracle(torch_dev, shape, mode):
     """Shapes that the default setting itself cuts (vattn_set_split_tiles(1)),

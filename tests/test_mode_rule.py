@@ -24,8 +24,13 @@ def lib():
 @pytest.mark.parametrize("shape,aligned,mode", [
     ((8, 16, 2304, 64), 1, SINGLE),      # the benchmark workload
     ((8, 16, 2304, 64), 0, TWO),         # unaligned pointers: neither one-kernel mode
-    ((4, 16, 1024, 64), 1, DIRECT),      # <= 2048 patches, head_dim 33..64
-    ((4, 16, 2048, 64), 1, DIRECT),
+    ((4, 16, 1024, 64), 1, DIRECT),      # <= 1536 patches, head_dim 33..64
+    ((8, 16, 1536, 64), 1, DIRECT),
+    ((8, 16, 1537, 64), 1, SINGLE),      # 896 work tiles: more than two rounds of 152
+    ((4, 16, 2048, 64), 1, SINGLE),      # 512 work tiles
+    ((2, 19, 2048, 64), 1, DIRECT),      # 304 work tiles: two rounds
+    ((2, 20, 2048, 64), 1, SINGLE),      # 320 work tiles
+    ((1, 16, 2048, 64), 1, DIRECT),
     ((4, 16, 2049, 64), 1, SINGLE),
     ((1, 16, 4100, 72), 1, TWO),         # head_dim past 64
     ((1, 16, 4100, 62), 1, TWO),         # head_dim not a multiple of 4
@@ -37,38 +42,52 @@ def lib():
     ((2, 2, 130, 128), 1, TWO),
 ])
 def test_mode_rule_on_a_capable_device(lib, shape, aligned, mode):
-    assert _lib.forward_mode_for(*shape, aligned, 1, 1) == mode
+    assert _lib.forward_mode_for(*shape, aligned, 1, 1, 152) == mode
 
 
 @pytest.mark.parametrize("coop,blocks", [(0, 1), (1, 0), (0, 0)])
 def test_single_kernel_needs_cooperative_launch_and_a_resident_block(lib, coop, blocks):
     # where the single kernel would run, a device without the facts gets two kernels
-    assert _lib.forward_mode_for(8, 16, 2304, 64, 1, coop, blocks) == TWO
-    assert _lib.forward_mode_for(1, 2, 129, 32, 1, coop, blocks) == TWO
+    assert _lib.forward_mode_for(8, 16, 2304, 64, 1, coop, blocks, 152) == TWO
+    assert _lib.forward_mode_for(1, 2, 129, 32, 1, coop, blocks, 152) == TWO
     # the other modes do not depend on them
-    assert _lib.forward_mode_for(4, 16, 1024, 64, 1, coop, blocks) == DIRECT
-    assert _lib.forward_mode_for(1, 16, 4100, 72, 1, coop, blocks) == TWO
+    assert _lib.forward_mode_for(4, 16, 1024, 64, 1, coop, blocks, 152) == DIRECT
+    assert _lib.forward_mode_for(1, 16, 4100, 72, 1, coop, blocks, 152) == TWO
+    # from 1537 to 2048 patches the direct kernel stands in for the single one
+    assert _lib.forward_mode_for(4, 16, 2048, 64, 1, coop, blocks, 152) == DIRECT
 
 
 def test_process_wide_switch(lib):
     prev = _lib.set_single_kernel(False)
     try:
         assert prev is True
-        assert _lib.forward_mode_for(8, 16, 2304, 64, 1, 1, 1) == TWO
-        assert _lib.forward_mode_for(4, 16, 1024, 64, 1, 1, 1) == DIRECT
+        assert _lib.forward_mode_for(8, 16, 2304, 64, 1, 1, 1, 152) == TWO
+        assert _lib.forward_mode_for(4, 16, 1024, 64, 1, 1, 1, 152) == DIRECT
     finally:
         assert _lib.set_single_kernel(True) is False
-    assert _lib.forward_mode_for(8, 16, 2304, 64, 1, 1, 1) == SINGLE
+    assert _lib.forward_mode_for(8, 16, 2304, 64, 1, 1, 1, 152) == SINGLE
+
+
+def test_rounds_follow_the_multiprocessor_count(lib):
+    # 512 work tiles at 2048 patches: more than two rounds of 152 blocks, at
+    # most two of 256
+    assert _lib.forward_mode_for(4, 16, 2048, 64, 1, 1, 1, 152) == SINGLE
+    assert _lib.forward_mode_for(4, 16, 2048, 64, 1, 1, 1, 256) == DIRECT
+    # up to 1536 patches the direct kernel whatever the count
+    assert _lib.forward_mode_for(64, 16, 1536, 64, 1, 1, 1, 8) == DIRECT
+    with pytest.raises(vef.VattnError) as e:
+        _lib.forward_mode_for(4, 16, 2048, 64, 1, 1, 1, 0)
+    assert e.value.status == 1
 
 
 def test_empty_and_invalid(lib):
-    assert _lib.forward_mode_for(0, 16, 2304, 64, 1, 1, 1) == _lib.MODE_NONE
-    assert _lib.forward_mode_for(8, 16, 0, 64, 1, 1, 1) == _lib.MODE_NONE
+    assert _lib.forward_mode_for(0, 16, 2304, 64, 1, 1, 1, 152) == _lib.MODE_NONE
+    assert _lib.forward_mode_for(8, 16, 0, 64, 1, 1, 1, 152) == _lib.MODE_NONE
     with pytest.raises(vef.VattnError) as e:
-        _lib.forward_mode_for(8, 16, 2304, 129, 1, 1, 1)
+        _lib.forward_mode_for(8, 16, 2304, 129, 1, 1, 1, 152)
     assert e.value.status == 2
     with pytest.raises(vef.VattnError) as e:
-        _lib.forward_mode_for(8, -1, 2304, 64, 1, 1, 1)
+        _lib.forward_mode_for(8, -1, 2304, 64, 1, 1, 1, 152)
     assert e.value.status == 1
 
 

@@ -22,6 +22,7 @@ import pytest
 
 import oracle
 import vision_encoder_flash_gb300 as vef
+from vision_encoder_flash_gb300 import _lib
 from vattn_inputs import WORKLOADS, make_inputs, workload_inputs
 
 pytestmark = pytest.mark.gpu
@@ -262,9 +263,10 @@ def test_host_tensors_round_trip(torch_dev):
 
 
 # The direct f32 path (one kernel that rounds q, k, v to f16 in shared
-# memory): 128 < n_patches <= 2048, head_dim 33..64 and a multiple of 4,
-# 16-byte aligned inputs.  Ragged ends, the 2048 limit, and enough heads that
-# every block takes several work tiles (40 heads x 4 query blocks > 152).
+# memory): 128 < n_patches <= 2048 (past 1536 only for up to two rounds of
+# work tiles), head_dim 33..64 and a multiple of 4, 16-byte aligned inputs.
+# Ragged ends, the 2048 limit, and enough heads that every block takes
+# several work tiles (40 heads x 4 query blocks > 152).
 DIRECT = [(1, 3, n, d) for d in (36, 44, 52, 64) for n in (129, 255, 256, 257, 1000, 2048)]
 DIRECT += [(2, 40, 1000, 64), (1, 160, 300, 40)]
 
@@ -311,8 +313,10 @@ def test_direct_and_staged_paths_agree_bitwise(torch_dev, shape):
 
 @pytest.mark.parametrize("n", [2048, 2049])
 def test_direct_path_limit(torch_dev, n):
-    # 2048 patches take the single kernel, 2049 the two passes: both correct
+    # one head: 2048 patches take the direct kernel, 2049 the single kernel
     q, k, v = make_inputs(1, 1, n, 64, seed=5200 + n)
+    assert _lib.forward_mode_for(1, 1, n, 64, 1, 1, 1, 152) == (
+        _lib.MODE_DIRECT if n == 2048 else _lib.MODE_SINGLE_KERNEL)
     got = run_gpu(torch_dev, q, k, v)
     assert_parity(got, oracle.forward(q, k, v), f"limit N={n}", rel_l2=2 * MAX_REL_L2)
 

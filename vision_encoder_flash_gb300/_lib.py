@@ -61,7 +61,7 @@ def load_library():
     lib.vattn_forward_mode.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ip]
     lib.vattn_forward_mode.restype = ctypes.c_int
     lib.vattn_forward_mode_for.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
-                                           ctypes.c_int, ip]
+                                           ctypes.c_int, ctypes.c_int, ip]
     lib.vattn_forward_mode_for.restype = ctypes.c_int
     lib.vattn_set_single_kernel.argtypes = [ctypes.c_int]
     lib.vattn_set_single_kernel.restype = ctypes.c_int
@@ -207,13 +207,14 @@ def forward_mode(q_ptr, k_ptr, v_ptr, out_ptr, batch, n_heads, n_patches, head_d
 
 
 def forward_mode_for(batch, n_heads, n_patches, head_dim, aligned, cooperative_launch,
-                     blocks_per_sm) -> int:
+                     blocks_per_sm, n_sms) -> int:
     """The mode rule with the device facts passed in (vattn_forward_mode_for,
-    no CUDA call); raises on argument errors."""
+    no CUDA call; n_sms: the device's multiprocessors); raises on argument
+    errors."""
     mode = ctypes.c_int(-1)
     _check(load_library().vattn_forward_mode_for(batch, n_heads, n_patches, head_dim, int(aligned),
                                                  int(cooperative_launch), int(blocks_per_sm),
-                                                 ctypes.byref(mode)))
+                                                 int(n_sms), ctypes.byref(mode)))
     return int(mode.value)
 
 

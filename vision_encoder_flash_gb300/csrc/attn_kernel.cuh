@@ -570,9 +570,9 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
     // Ring tile n (slot n % 2) is the n-th of the sequence warp 0 loads; it
     // goes to the K or V stage of its key tile or to a Q tile once the MMAs
     // are done with that buffer.  Warp cw rounds rows [32 cw, 32 cw + 32):
-    // per step two rows, 16 lanes per row, four f32 columns per lane, into
-    // the 128-byte-swizzled f16 layout TMA would have written (16-byte unit
-    // u of row r at u ^ (r & 7)).
+    // per step four rows, 8 lanes per row, eight f32 columns per lane, into
+    // one 16-byte unit of the 128-byte-swizzled f16 layout TMA would have
+    // written (unit u of row r at u ^ (r & 7)).
     const int cw = warp - (4 + 4 * NQ);
     int64_t n = 0;
     auto convert = [&](uint32_t dst, int full_bar) -> bool {
@@ -581,15 +581,18 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
                        kSiteConvert))
         return false;
       const uint32_t src = base_s + P::kOffF32 + static_cast<uint32_t>(slot * P::kF32TileBytes);
-      const int c4 = lane & 15;  // f32 columns 4 c4 .. 4 c4 + 3
-#pragma unroll 4
-      for (int it = 0; it < 16; ++it) {
-        const int r = 32 * cw + 2 * it + (lane >> 4);
-        const float4 x = ptx::ld_shared_v4(src + static_cast<uint32_t>(r * 256 + c4 * 16));
-        const uint32_t unit = static_cast<uint32_t>((c4 >> 1) ^ (r & 7));
-        ptx::st_shared_v2(dst + static_cast<uint32_t>(r * 128) + unit * 16u +
-                              static_cast<uint32_t>(c4 & 1) * 8u,
-                          ptx::pack_half2(x.x, x.y), ptx::pack_half2(x.z, x.w));
+      const int u = lane & 7;  // f32 columns 8 u .. 8 u + 7 = 16-byte f16 unit u
+#pragma unroll 2
+      for (int it = 0; it < 8; ++it) {
+        const int r = 32 * cw + 4 * it + (lane >> 3);
+        const uint32_t a = src + static_cast<uint32_t>(r * 256 + u * 32);
+        const float4 x0 = ptx::ld_shared_v4(a);
+        const float4 x1 = ptx::ld_shared_v4(a + 16u);
+        ptx::st_shared_v4(dst + static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4)),
+                          __uint_as_float(ptx::pack_half2(x0.x, x0.y)),
+                          __uint_as_float(ptx::pack_half2(x0.z, x0.w)),
+                          __uint_as_float(ptx::pack_half2(x1.x, x1.y)),
+                          __uint_as_float(ptx::pack_half2(x1.z, x1.w)));
       }
       ptx::fence_proxy_async_smem();  // the tensor core reads what was written
       __syncwarp();

@@ -593,33 +593,58 @@ vattn_status single_kernel_facts(int device, int* cooperative, int* blocks_per_s
   return VATTN_OK;
 }
 
+// Up to this many patches a direct shape always takes the direct kernel;
+// from 1537 to 2048 patches only while its work tiles fill at most two
+// rounds of the grid.  Beyond that the single kernel, which rounds each key
+// tile once per head instead of once per query block, measured faster
+// (GB300, whole calls: 8 x 16 heads x 2048 x 64 161.6 against 170.1 us,
+// 8 x 16 x 1792 x 64 128.5 against 130.9, 4 x 16 x 2048 x 64 97.3 against
+// 99.3), and the direct kernel below it (8 x 16 x 1536 x 64 113.6 against
+// 114.9, 2 x 16 x 2048 x 64 52.1 against 56.1, 1 x 16 x 2048 x 64 28.6
+// against 34.7).
+constexpr int kDirectAlwaysMaxN = 1536;
+
 // The kernels a vattn_forward call on a non-empty, valid problem runs, from
-// its sizes, whether q, k and v are all 16-byte aligned, and the device
-// facts above (single_allowed: the caller and the process-wide switch allow
-// the single cooperative kernel).
-vattn_mode forward_mode_rule(int N, int D, bool all_aligned16, bool single_allowed,
-                             int cooperative, int blocks_per_sm) {
+// its sizes (n_tiles: its work tiles, batch*n_heads * query blocks), whether
+// q, k and v are all 16-byte aligned, and the device facts: n_sms
+// multiprocessors (the grid) and the single kernel's facts above
+// (single_allowed: the caller and the process-wide switch allow it).
+vattn_mode forward_mode_rule(int N, int D, long long n_tiles, int n_sms, bool all_aligned16,
+                             bool single_allowed, int cooperative, int blocks_per_sm) {
   const int d_pad = (D + 15) & ~15;
-  if (all_aligned16 && direct_shape(N, D)) return VATTN_MODE_DIRECT;
   const int nkb = d_pad <= 64 ? 1 : 2;
   const bool q_f32 = nkb == 1 && query_tiles(N, d_pad) == 2 && D % 4 == 0;
-  if (single_allowed && all_aligned16 && q_f32 && cooperative != 0 && blocks_per_sm >= 1)
-    return VATTN_MODE_SINGLE_KERNEL;
-  return VATTN_MODE_TWO_KERNELS;
+  const bool single = single_allowed && all_aligned16 && q_f32 && cooperative != 0 &&
+                      blocks_per_sm >= 1;
+  if (all_aligned16 && direct_shape(N, D)) {
+    if (single && N > kDirectAlwaysMaxN && n_tiles > 2LL * n_sms) return VATTN_MODE_SINGLE_KERNEL;
+    return VATTN_MODE_DIRECT;
+  }
+  return single ? VATTN_MODE_SINGLE_KERNEL : VATTN_MODE_TWO_KERNELS;
+}
+
+// Work tiles of a problem: batch*n_heads * query blocks of nq query tiles.
+long long work_tiles(long long bh, int N, int D) {
+  const int nq = query_tiles(N, (D + 15) & ~15);
+  return bh * ((N + vattn::kBM * nq - 1) / (vattn::kBM * nq));
 }
 
 // The mode a call takes on `device` (sizes and pointers already checked).
-vattn_status forward_mode_on(int device, const float* q, const float* k, const float* v, int N,
-                             int D, bool single_kernel, vattn_mode* mode) {
-  int coop = 0, blocks = 0;
+vattn_status forward_mode_on(int device, const float* q, const float* k, const float* v,
+                             int64_t bh, int N, int D, bool single_kernel, vattn_mode* mode) {
+  int coop = 0, blocks = 0, sms = 0;
+  vattn_status st = sm_count(device, &sms);
+  if (st != VATTN_OK) return st;
+  const long long n_tiles = work_tiles(bh, N, D);
   const bool allowed = single_kernel && g_single_kernel_allowed.load(std::memory_order_relaxed) != 0;
   const bool al = aligned16(q, k, v);
   // the facts are read only when the rule could take the single kernel
-  if (allowed && forward_mode_rule(N, D, al, true, 1, 1) == VATTN_MODE_SINGLE_KERNEL) {
-    const vattn_status st = single_kernel_facts(device, &coop, &blocks);
+  if (allowed &&
+      forward_mode_rule(N, D, n_tiles, sms, al, true, 1, 1) == VATTN_MODE_SINGLE_KERNEL) {
+    st = single_kernel_facts(device, &coop, &blocks);
     if (st != VATTN_OK) return st;
   }
-  *mode = forward_mode_rule(N, D, al, allowed, coop, blocks);
+  *mode = forward_mode_rule(N, D, n_tiles, sms, al, allowed, coop, blocks);
   return VATTN_OK;
 }
 
@@ -654,7 +679,7 @@ vattn_status plan_forward(int device, const float* q, const float* k, const floa
                           int N, int D, bool single_kernel, size_t max_sync_part_bytes,
                           ForwardPlan* out) {
   ForwardPlan pl;
-  vattn_status st = forward_mode_on(device, q, k, v, N, D, single_kernel, &pl.mode);
+  vattn_status st = forward_mode_on(device, q, k, v, bh, N, D, single_kernel, &pl.mode);
   if (st != VATTN_OK) return st;
   pl.N = N;
   pl.D = D;
@@ -1398,10 +1423,11 @@ const char* vattn_status_string(vattn_status status) {
 
 vattn_status vattn_forward_mode_for(int64_t batch, int64_t n_heads, int64_t n_patches,
                                     int64_t head_dim, int aligned, int cooperative_launch,
-                                    int blocks_per_sm, int* mode) {
+                                    int blocks_per_sm, int n_sms, int* mode) {
   g_last_error[0] = '\0';
   if (!mode) return fail(VATTN_ERR_INVALID_ARG, "null mode pointer");
   *mode = VATTN_MODE_NONE;
+  if (n_sms < 1) return fail(VATTN_ERR_INVALID_ARG, "n_sms must be at least 1");
   const vattn_status chk = check_attention_sizes(batch, n_heads, n_patches, head_dim);
   if (chk != VATTN_OK) return chk;
   if (batch != 0 && n_heads > INT64_MAX / batch)
@@ -1410,8 +1436,9 @@ vattn_status vattn_forward_mode_for(int64_t batch, int64_t n_heads, int64_t n_pa
   if (n_patches > INT32_MAX || batch * n_heads > INT32_MAX)
     return fail(VATTN_ERR_UNSUPPORTED, "n_patches and batch*n_heads must fit in 32 bits");
   const bool allowed = g_single_kernel_allowed.load(std::memory_order_relaxed) != 0;
-  *mode = forward_mode_rule(static_cast<int>(n_patches), static_cast<int>(head_dim), aligned != 0,
-                            allowed, cooperative_launch, blocks_per_sm);
+  const int N = static_cast<int>(n_patches), D = static_cast<int>(head_dim);
+  *mode = forward_mode_rule(N, D, work_tiles(batch * n_heads, N, D), n_sms, aligned != 0, allowed,
+                            cooperative_launch, blocks_per_sm);
   return VATTN_OK;
 }
 
@@ -1454,7 +1481,7 @@ vattn_status vattn_forward_mode(const float* q, const float* k, const float* v, 
   const cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   vattn_mode m = VATTN_MODE_NONE;
-  const vattn_status st = forward_mode_on(device, q, k, v, static_cast<int>(n_patches),
+  const vattn_status st = forward_mode_on(device, q, k, v, bh, static_cast<int>(n_patches),
                                           static_cast<int>(head_dim), true, &m);
   if (st == VATTN_OK) *mode = m;
   return st;
