@@ -886,11 +886,22 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
           const uint32_t vb = base_s + P::kOffV + kv_stage(g) * P::kStageStride;
           const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColOStride;
           const uint32_t a = tmem + P::kColP + static_cast<uint32_t>(t) * P::kColPStride;
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
-                        ptx::smem_desc(vb + ks * 2048, kBoxBytes, 1024, ptx::kSwizzle128B),
-                        idesc_pv, (!first || ks > 0) ? 1u : 0u);
-            if constexpr (kAcc) {  // + Ph Vl + Pl Vh
+          if constexpr (!kAcc) {
+            // the V descriptor as 32-bit halves, one add per product (fewer
+            // instructions between the blocking issues); k-step ks starts
+            // 16 rows (2048 bytes) further on
+            constexpr uint32_t hi = ptx::smem_desc_hi(1024, ptx::kSwizzle128B);
+            const uint32_t vlo = ptx::smem_desc_lo(vb, kBoxBytes);
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks)
+              ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
+                          ptx::smem_desc_join(vlo + static_cast<uint32_t>(ks) * (2048u >> 4), hi),
+                          idesc_pv, (!first || ks > 0) ? 1u : 0u);
+          } else {
+            for (int ks = 0; ks < kBN / 16; ++ks) {  // Ph Vh + Ph Vl + Pl Vh
+              ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
+                          ptx::smem_desc(vb + ks * 2048, kBoxBytes, 1024, ptx::kSwizzle128B),
+                          idesc_pv, (!first || ks > 0) ? 1u : 0u);
               ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
                           ptx::smem_desc(vb + P::kPartBytes + ks * 2048, kBoxBytes, 1024,
                                          ptx::kSwizzle128B),
