@@ -189,9 +189,9 @@ __device__ __forceinline__ Piece piece_at(const volatile Sched* sp, int i, int T
 // kIn (two query tiles, head_dim <= 64 for kInF32 and kInF32Q): where the
 // operands come from.
 //   kInF16:  q, k, v f16 copies (the staging kernel's), TMA into the tiles;
-//   kInF32:  q, k, v f32 tiles [128 rows x 64 columns] into a ring of three
+//   kInF32:  q, k, v f32 tiles [128 rows x 64 columns] into a ring of two
 //            slots; a fourth warpgroup rounds them to f16 into the same
-//            swizzled tiles;
+//            swizzled tiles (three K/V stages);
 //   kInF32Q: k, v f16 copies; q f32 tiles into two slots (one per query
 //            tile), rounded to f16 by warp 3 once per work tile;
 //   kInStageKV: as kInF32Q, and a fourth warpgroup writes the f16 copies of
@@ -212,7 +212,7 @@ struct Plan {
   static constexpr int kPartBytes = kTileF16;      // offset of lo after hi
   static constexpr int kStageStride = kParts * kTileF16;
   static constexpr int kStages =  // K and V stages
-      kF32 ? 2 : (kStageKV ? 2 : (kF32Q ? 3 : (kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3)))));
+      kF32 ? 3 : (kStageKV ? 2 : (kF32Q ? 3 : (kAcc ? (NKB == 1 ? 3 : 1) : (NKB == 1 ? 5 : (NQ == 2 ? 2 : 3)))));
   // two query tiles with head_dim > 64: O needs 2 x 80..128 TMEM columns, so
   // the two tiles take turns with one P buffer
   static constexpr bool kSharedP = NQ == 2 && NKB == 2;
@@ -225,7 +225,7 @@ struct Plan {
   static constexpr int kOffEpi = kOffV + kStages * kStageStride;
   // f32 slots: the kInF32 ring; one per query tile for kInF32Q; and for
   // kInStageKV one more, slot NQ, for the k / v tiles being staged
-  static constexpr int kF32Slots = kF32 ? 3 : (kStageKV ? NQ + 1 : (kF32Q ? NQ : 0));
+  static constexpr int kF32Slots = kF32 ? 2 : (kStageKV ? NQ + 1 : (kF32Q ? NQ : 0));
   static constexpr int kF32TileBytes = kBM * 64 * 4;  // 128 rows x 64 f32, unswizzled
   static constexpr int kOffF32 = kOffEpi + kEpiBytes;
   static constexpr int kOffBar = kOffF32 + kF32Slots * kF32TileBytes;
