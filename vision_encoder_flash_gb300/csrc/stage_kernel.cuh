@@ -25,25 +25,44 @@ struct StageJob {
   __half* dst;
 };
 
-// n_jobs (2 or 3) tensors (a, b[, c]: q, k, v, or k and v alone when the
-// attention kernel rounds q itself) of n_rows x D each.  Thread i handles
-// 8-column chunks i, i + stride, ... of the concatenated
-// [n_jobs * n_rows, d_pad / 8] chunk grid.  vec: D % 8 == 0 and 16-byte
-// aligned sources -> two 16-byte loads per chunk; otherwise element loads.
+// A walk over the 8-column chunks c = row * cpr + ch of one tensor's
+// [n_rows, cpr] chunk grid: chunk c0, c0 + stride, ..., stepped by rows and
+// columns so that no chunk costs a division.
+struct ChunkWalk {
+  long long row;
+  int ch;
+  long long row_step;
+  int ch_step;
+  __device__ __forceinline__ ChunkWalk(long long c0, long long stride, int cpr)
+      : row(c0 / cpr), ch(static_cast<int>(c0 - (c0 / cpr) * cpr)), row_step(stride / cpr),
+        ch_step(static_cast<int>(stride - (stride / cpr) * cpr)) {}
+  __device__ __forceinline__ void next(int cpr) {
+    row += row_step;
+    ch += ch_step;
+    if (ch >= cpr) {
+      ch -= cpr;
+      ++row;
+    }
+  }
+};
+
+// gridDim.y (2 or 3) tensors (a, b[, c]: q, k, v, or k and v alone when the
+// attention kernel rounds q itself) of n_rows x D each, tensor blockIdx.y.
+// Thread i of a row of blocks handles the 8-column chunks i, i + stride, ...
+// of its tensor's [n_rows, d_pad / 8] chunk grid.  vec: D % 8 == 0 and
+// 16-byte aligned sources -> two 16-byte loads per chunk; otherwise element
+// loads.
 __global__ void __launch_bounds__(256) vattn_stage_kernel(StageJob a, StageJob b, StageJob c,
-                                                         int n_jobs, long long n_rows, int D,
-                                                         int d_pad, int vec) {
+                                                         long long n_rows, int D, int d_pad,
+                                                         int vec) {
   const int cpr = d_pad >> 3;
-  const long long chunks_per_tensor = n_rows * cpr;
-  const long long total = n_jobs * chunks_per_tensor;
+  const int which = static_cast<int>(blockIdx.y);
+  const StageJob job = which == 0 ? a : (which == 1 ? b : c);
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const int which = static_cast<int>(i / chunks_per_tensor);
-    const long long r = i - which * chunks_per_tensor;
-    const long long row = r / cpr;
-    const int ch = static_cast<int>(r - row * cpr);
-    const StageJob job = which == 0 ? a : (which == 1 ? b : c);
+  for (ChunkWalk w(static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x, stride, cpr);
+       w.row < n_rows; w.next(cpr)) {
+    const long long row = w.row;
+    const int ch = w.ch;
     const float* s = job.src + row * D + ch * 8;
     float x[8];
     if (vec && ch * 8 + 8 <= D) {
@@ -72,7 +91,7 @@ namespace vattn {
 // Two-term f16 split of q, k and v for the accurate mode:
 //   hi = f16(x), lo = f16(x - f32(hi))   (round to nearest even both times)
 // so x = hi + lo to about 2^-22 relative (f16 subnormals bound lo's error
-// at 2^-25 absolute).  Same layout and chunk decomposition as
+// at 2^-25 absolute).  Same layout, grid and chunk walk as
 // vattn_stage_kernel; `dst` of each job receives hi, `dst_lo` lo.
 struct SplitJob {
   const float* src;
@@ -84,16 +103,13 @@ __global__ void __launch_bounds__(256) vattn_stage_split_kernel(SplitJob a, Spli
                                                                long long n_rows, int D, int d_pad,
                                                                int vec) {
   const int cpr = d_pad >> 3;
-  const long long chunks_per_tensor = n_rows * cpr;
-  const long long total = 3 * chunks_per_tensor;
+  const int which = static_cast<int>(blockIdx.y);  // gridDim.y = 3: q, k, v
+  const SplitJob job = which == 0 ? a : (which == 1 ? b : c);
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const int which = static_cast<int>(i / chunks_per_tensor);
-    const long long r = i - which * chunks_per_tensor;
-    const long long row = r / cpr;
-    const int ch = static_cast<int>(r - row * cpr);
-    const SplitJob job = which == 0 ? a : (which == 1 ? b : c);
+  for (ChunkWalk w(static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x, stride, cpr);
+       w.row < n_rows; w.next(cpr)) {
+    const long long row = w.row;
+    const int ch = w.ch;
     const float* s = job.src + row * D + ch * 8;
     float x[8];
     if (vec && ch * 8 + 8 <= D) {

@@ -670,6 +670,16 @@ struct ForwardPlan {
 
 size_t round256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 
+// Blocks of 256 threads per tensor for the staging kernels (one row of
+// blocks per tensor, n_tensors rows): one thread per 8-column chunk, at most
+// 16 blocks per multiprocessor of 152 in all rows together (the threads then
+// walk several chunks each).
+unsigned stage_blocks(long long chunks_per_tensor, unsigned n_tensors) {
+  const long long cap = 152LL * 16 / n_tensors;
+  const long long blocks = (chunks_per_tensor + 255) / 256;
+  return static_cast<unsigned>(blocks < cap ? blocks : cap);
+}
+
 // single_kernel: the caller allows the single cooperative kernel (the
 // host-buffer entry point does not); max_sync_part_bytes: room for the sync
 // words and partial slots together (a cut schedule is taken only if they
@@ -780,18 +790,16 @@ vattn_status run_forward(const ForwardPlan& pl, const float* q, const float* k, 
   const uintptr_t src_or = (q_f32 ? 0u : reinterpret_cast<uintptr_t>(q)) |
                            reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v);
   const int vec = (D % 8 == 0) && (src_or & 15u) == 0;
-  const int n_jobs = q_f32 ? 2 : 3;
-  const long long chunks = n_jobs * rows * (d_pad / 8);
-  const long long blocks = (chunks + 255) / 256;
-  const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
+  const unsigned n_jobs = q_f32 ? 2u : 3u;
+  const dim3 stage_grid(stage_blocks(rows * (d_pad / 8), n_jobs), n_jobs);
   if (q_f32)
     vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
-        vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, vattn::StageJob{nullptr, nullptr}, 2, rows,
+        vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, vattn::StageJob{nullptr, nullptr}, rows,
         D, d_pad, vec);
   else
     vattn::vattn_stage_kernel<<<stage_grid, 256, 0, stream>>>(
-        vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, 3, rows, D,
-        d_pad, vec);
+        vattn::StageJob{q, q16}, vattn::StageJob{k, k16}, vattn::StageJob{v, v16}, rows, D, d_pad,
+        vec);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
   const unsigned g = static_cast<unsigned>(grid);
@@ -1175,9 +1183,7 @@ vattn_status vattn_forward_accurate(const float* q, const float* k, const float*
     const int vec = (D % 8 == 0) &&
                     ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                       reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
-    const long long chunks = 3LL * rows * (d_pad / 8);
-    const long long blocks = (chunks + 255) / 256;
-    const unsigned stage_grid = static_cast<unsigned>(blocks < 152LL * 16 ? blocks : 152LL * 16);
+    const dim3 stage_grid(stage_blocks(rows * (d_pad / 8), 3), 3);
     vattn::vattn_stage_split_kernel<<<stage_grid, 256, 0, stream>>>(
         vattn::SplitJob{q, part[0], part[3]}, vattn::SplitJob{k, part[1], part[4]},
         vattn::SplitJob{v, part[2], part[5]}, rows, D, d_pad, vec);
