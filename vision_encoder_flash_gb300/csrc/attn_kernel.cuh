@@ -51,8 +51,8 @@
 //     (40).
 // TMEM columns (512): S buffers [0,128) and [128,256); with two query tiles
 // P0, P1 at 256, 320 and O0, O1 at 384, 448 (head_dim <= 64), or one P
-// buffer at 256 that the two tiles take in turn and O0, O1 at 320, 416
-// (head_dim 65..96); with one query tile P at 256 and O at 320 (head_dim
+// buffer at 256 that the two tiles take in turn, half (64 keys) by half, and
+// O0, O1 at 320, 416 (head_dim 65..96); with one query tile P at 256 and O at 320 (head_dim
 // <= 128; the accurate mode: P hi 256, P lo 320, O 384).
 // Every wait is bounded: on timeout the block records the wait site in
 // g_vattn_status, raises a shared abort flag so the other roles leave their
@@ -276,7 +276,9 @@ enum Bar : int {
   kBarF32Full = 31,   // [4] f32 ring slot landed           (1 + tx)
   kBarF32Empty = 35,  // [4] f32 ring slot read (one per converter warp)
   kBarQFull1 = 39,    // kInF32Q: Q tile 1 rounded (Q tile 0: kBarQFull)
-  kNumBars = 40,
+  kBarPHalf = 40,     // [2] shared P: first half (keys 0..63) of P written (one per softmax warp)
+  kBarOHalf = 42,     // [2] shared P: P.V of the first half complete (commit)
+  kNumBars = 44,
 };
 constexpr int kTmemSlotOff = kNumBars * 8;   // u32 TMEM base address
 constexpr int kAbortOff = kTmemSlotOff + 4;  // u32 abort flag
@@ -438,6 +440,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
       ptx::mbar_init(bar(kBarSFree + i), NQ == 2 ? 8 : 4);
       ptx::mbar_init(bar(kBarPFull + i), P::kSharedP ? 4 : 4 * NQ);
       ptx::mbar_init(bar(kBarODone + i), 1);
+      ptx::mbar_init(bar(kBarPHalf + i), 4);
+      ptx::mbar_init(bar(kBarOHalf + i), 1);
     }
     ptx::mbar_init(bar(kBarMmaDone), 2);
     *abort_flag = 0;
@@ -882,7 +886,8 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
       } else if (lane == 0 && warp == 2) {
         // O_t += P_t V_g
         const uint32_t idesc_pv = ptx::idesc_f16_f32(kBM, static_cast<uint32_t>(p.d_pad), true);
-        auto issue_pv = [&](int t, int64_t g, bool first) {
+        // k-steps [ks0, ks1) of O_t += P_t V_g, then a commit on `done`
+        auto issue_pv = [&](int t, int64_t g, bool first, int ks0, int ks1, int done) {
           const uint32_t vb = base_s + P::kOffV + kv_stage(g) * P::kStageStride;
           const uint32_t d = tmem + P::kColO + static_cast<uint32_t>(t) * P::kColOStride;
           const uint32_t a = tmem + P::kColP + static_cast<uint32_t>(t) * P::kColPStride;
@@ -892,13 +897,12 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
             // 16 rows (2048 bytes) further on
             constexpr uint32_t hi = ptx::smem_desc_hi(1024, ptx::kSwizzle128B);
             const uint32_t vlo = ptx::smem_desc_lo(vb, kBoxBytes);
-#pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks)
+            for (int ks = ks0; ks < ks1; ++ks)
               ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
                           ptx::smem_desc_join(vlo + static_cast<uint32_t>(ks) * (2048u >> 4), hi),
                           idesc_pv, (!first || ks > 0) ? 1u : 0u);
           } else {
-            for (int ks = 0; ks < kBN / 16; ++ks) {  // Ph Vh + Ph Vl + Pl Vh
+            for (int ks = ks0; ks < ks1; ++ks) {  // Ph Vh + Ph Vl + Pl Vh
               ptx::mma_ts(d, a + static_cast<uint32_t>(ks) * 8u,
                           ptx::smem_desc(vb + ks * 2048, kBoxBytes, 1024, ptx::kSwizzle128B),
                           idesc_pv, (!first || ks > 0) ? 1u : 0u);
@@ -911,7 +915,7 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
                           idesc_pv, 1u);
             }
           }
-          ptx::mma_commit(bar(kBarODone + t));
+          ptx::mma_commit(bar(done));
         };
         bool ok = true;
         int g = 0;  // key tiles of this block so far
@@ -922,17 +926,23 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
             // P of key tile g written (for the first key tile of a tile this
             // also tells that the softmax has read the previous tile's O)
             if constexpr (P::kSharedP) {
-              // the two query tiles take turns with the P buffer
+              // the two query tiles take turns with the P buffer, half by
+              // half: tile t's first half (keys 0..63) goes to the tensor
+              // core as soon as it is written, while the softmax writes the
+              // second half once the other tile's P V has read it
               for (int t = 0; ok && t < NQ; ++t) {
+                if (!(ok = w.wait(bar(kBarPHalf + t), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
+                ptx::tc_fence_after();
+                issue_pv(t, g, j == pc.j0, 0, kBN / 32, kBarOHalf + t);
                 if (!(ok = w.wait(bar(kBarPFull + t), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
                 ptx::tc_fence_after();
-                issue_pv(t, g, j == pc.j0);
+                issue_pv(t, g, j == pc.j0, kBN / 32, kBN / 16, kBarODone + t);
               }
               if (!ok) break;
             } else {
               if (!(ok = w.wait(bar(kBarPFull), static_cast<uint32_t>(g & 1), kSiteMmaP))) break;
               ptx::tc_fence_after();
-              for (int t = 0; t < NQ; ++t) issue_pv(t, g, j == pc.j0);
+              for (int t = 0; t < NQ; ++t) issue_pv(t, g, j == pc.j0, 0, kBN / 16, kBarODone + t);
             }
             ptx::mma_commit(bar(kBarVEmpty + kv_stage(g)));
           }
@@ -1021,14 +1031,16 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
         const float2 s01 = __fadd2_rn(acc[0], acc[1]);
         const float2 s23 = __fadd2_rn(acc[2], acc[3]);
         l = fmaf(l, alpha, (s01.x + s01.y) + (s23.x + s23.y));
+        const int64_t gw = t == 0 ? g - 1 : g;  // shared P: the other tile's P V before ours
         if (P::kSharedP) {
-          // one P buffer, used by (tile 0, g), (tile 1, g), (tile 0, g + 1), ...:
-          // tile 0 waits for the P V of (1, g - 1), tile 1 for that of (0, g).
-          // One thread issues them in that order, so either also means the
-          // tile's own previous P V has finished (O final for a rescale).
-          const int64_t gw = t == 0 ? g - 1 : g;
+          // one P buffer, used by (tile 0, g), (tile 1, g), (tile 0, g + 1), ...,
+          // half by half: tile 0 writes its first half once the P V of (1,
+          // g - 1) has read that half, tile 1 once that of (0, g) has.  One
+          // thread issues the products in that order and a commit tracks all
+          // earlier ones, so this also means the tile's own previous P V has
+          // finished (O final for a rescale).
           if (gw >= 0) {
-            if (!(ok = w.wait_warp(bar(kBarODone + (1 - t)), static_cast<uint32_t>(gw & 1),
+            if (!(ok = w.wait_warp(bar(kBarOHalf + (1 - t)), static_cast<uint32_t>(gw & 1),
                                    kSiteSoftO)))
               break;
             ptx::tc_fence_after();
@@ -1053,17 +1065,37 @@ __global__ void __launch_bounds__(Plan<NQ, NKB, kAcc, kIn>::kThreads, 1)
             }
           }
         }
+        if constexpr (P::kSharedP) {
+          // first half, then (once the other tile's P V has read the whole
+          // buffer) the second half
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk[c]);
-        if constexpr (kAcc) {
+          for (int c = 0; c < 2; ++c) ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk[c]);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          warp_arrive(bar(kBarPHalf + t));
+          if (gw >= 0) {
+            if (!(ok = w.wait_warp(bar(kBarODone + (1 - t)), static_cast<uint32_t>(gw & 1),
+                                   kSiteSoftO)))
+              break;
+            ptx::tc_fence_after();
+          }
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            ptx::tmem_st_32x32b_x16(tmem + lane_addr + P::kColPlo + c * 16, pkl[c]);
+          for (int c = 2; c < 4; ++c) ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk[c]);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          warp_arrive(bar(kBarPFull + t));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ptx::tmem_st_32x32b_x16(p_addr + c * 16, pk[c]);
+          if constexpr (kAcc) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              ptx::tmem_st_32x32b_x16(tmem + lane_addr + P::kColPlo + c * 16, pkl[c]);
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          warp_arrive(bar(kBarPFull));
         }
-
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        warp_arrive(bar(kBarPFull + (P::kSharedP ? t : 0)));
       }
       if (!ok) break;
       // ---- epilogue of the tile: out = O / l for the rows < n_patches.  The
