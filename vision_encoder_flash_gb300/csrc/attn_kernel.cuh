@@ -51,9 +51,10 @@
 //     (40).
 // TMEM columns (512): S buffers [0,128) and [128,256); with two query tiles
 // P0, P1 at 256, 320 and O0, O1 at 384, 448 (head_dim <= 64), or one P
-// buffer at 256 that the two tiles take in turn, half (64 keys) by half, and
-// O0, O1 at 320, 416 (head_dim 65..96); with one query tile P at 256 and O at 320 (head_dim
-// <= 128; the accurate mode: P hi 256, P lo 320, O 384).
+// buffer at 256 that the two tiles take in turn, half (64 keys) by half,
+// and O0, O1 at 320, 416 (head_dim 65..96); with one query tile P at 256
+// and O at 320 (head_dim <= 128; the accurate mode: P hi 256, P lo 320, O
+// 384).
 // Every wait is bounded: on timeout the block records the wait site in
 // g_vattn_status, raises a shared abort flag so the other roles leave their
 // loops, drains its own TMA copies and MMAs, frees TMEM and exits.
